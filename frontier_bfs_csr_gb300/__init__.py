@@ -1,0 +1,294 @@
+"""Level-synchronous frontier BFS over CSR on one GB300 (sm_103a).
+
+This package is a thin ctypes binding over the C-ABI library
+``libbfs_csr.so`` (declared in ``include/bfs_csr.h``). Every step of a search
+runs in that library's CUDA kernels; this module only marshals arguments.
+PyTorch supplies device memory and streams. There is no CPU fallback: if the
+library has not been built (``python frontier_bfs_csr_gb300/build.py`` or
+``__graft_entry__.build()``), importing the binding fails.
+
+The functions below carry the C names. :class:`BfsCsr` wraps a handle for
+the common case of torch tensors on the current device.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libbfs_csr.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        "libbfs_csr.so is not built (expected at %s); run "
+        "`python frontier_bfs_csr_gb300/build.py`" % LIB_PATH)
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+# ------------------------------------------------------------------ constants
+BFS_CSR_OK = 0
+BFS_CSR_EINVAL = 1
+BFS_CSR_ENOMEM = 2
+BFS_CSR_ECUDA = 3
+BFS_CSR_ETIMEOUT = 4
+BFS_CSR_EUNSUPPORTED = 5
+BFS_CSR_EDEVICE = 6
+
+BFS_CSR_DIR_AUTO, BFS_CSR_DIR_PUSH, BFS_CSR_DIR_PULL = 0, 1, 2
+BFS_CSR_ADV_AUTO, BFS_CSR_ADV_BINNED, BFS_CSR_ADV_MERGE_PATH = 0, 1, 2
+BFS_CSR_DISC_BITMAP, BFS_CSR_DISC_CAS = 0, 1
+BFS_CSR_LOOP_PERSISTENT, BFS_CSR_LOOP_HOST = 0, 1
+
+EXPORTED = [
+    "bfs_csr_default_options", "bfs_csr_workspace_bytes", "bfs_csr_create", "bfs_csr_run",
+    "bfs_csr_run_init", "bfs_csr_run_levels",
+    "bfs_csr_sync", "bfs_csr_level_stats", "bfs_csr_create_host", "bfs_csr_run_host",
+    "bfs_csr_destroy", "bfs_csr_status_string", "bfs_csr_last_cuda_error",
+]
+
+
+class bfs_csr_options(ctypes.Structure):
+    _fields_ = [
+        ("direction", ctypes.c_int32),
+        ("advance", ctypes.c_int32),
+        ("discovery", ctypes.c_int32),
+        ("loop_mode", ctypes.c_int32),
+        ("small_max_degree", ctypes.c_int32),
+        ("cta_min_degree", ctypes.c_int32),
+        ("merge_path_min_frontier", ctypes.c_int32),
+        ("binned_max_degree", ctypes.c_int32),
+        ("pull_ratio", ctypes.c_double),
+        ("max_depth", ctypes.c_int32),
+        ("validate", ctypes.c_int32),
+        ("block_threads", ctypes.c_int32),
+        ("grid_blocks", ctypes.c_int32),
+        ("barrier_timeout_ns", ctypes.c_int64),
+        ("test_unreachable_barrier", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 7),
+    ]
+
+
+class bfs_csr_level_stat(ctypes.Structure):
+    _fields_ = [
+        ("level", ctypes.c_int32),
+        ("direction", ctypes.c_int32),
+        ("advance", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+        ("frontier", ctypes.c_int64),
+        ("frontier_edges", ctypes.c_int64),
+        ("unvisited", ctypes.c_int64),
+        ("max_degree", ctypes.c_int64),
+        ("t_start_ns", ctypes.c_int64),
+    ]
+
+
+_vp, _i64, _i32, _sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+_opt_p = ctypes.POINTER(bfs_csr_options)
+_sig = {
+    "bfs_csr_default_options": ([_opt_p], _i32),
+    "bfs_csr_workspace_bytes": ([_i64, _i64, _i32, _opt_p, ctypes.POINTER(_sz)], _i32),
+    "bfs_csr_create": ([ctypes.POINTER(_vp), _i64, _i64, _vp, _i32, _vp, _i32, _vp, _sz, _opt_p,
+                        _vp], _i32),
+    "bfs_csr_run": ([_vp, _i64, _vp, _vp, _vp, _vp], _i32),
+    "bfs_csr_run_init": ([_vp, _i64, _vp, _vp, _vp], _i32),
+    "bfs_csr_run_levels": ([_vp, _vp, _vp], _i32),
+    "bfs_csr_sync": ([_vp, _vp, ctypes.POINTER(ctypes.c_int32)], _i32),
+    "bfs_csr_level_stats": ([_vp, ctypes.POINTER(bfs_csr_level_stat), ctypes.c_int32,
+                             ctypes.POINTER(ctypes.c_int32)], _i32),
+    "bfs_csr_create_host": ([ctypes.POINTER(_vp), _i64, _i64, _vp, _i32, _vp, _i32, _opt_p, _vp],
+                            _i32),
+    "bfs_csr_run_host": ([_vp, _i64, _vp, _vp, _vp, _vp, _vp, _vp], _i32),
+    "bfs_csr_destroy": ([_vp], _i32),
+    "bfs_csr_status_string": ([_i32], ctypes.c_char_p),
+    "bfs_csr_last_cuda_error": ([_vp], _i32),
+}
+for _name, (_args, _res) in _sig.items():
+    _f = getattr(_lib, _name)
+    _f.argtypes = _args
+    _f.restype = _res
+    globals()[_name] = _f
+
+
+class BfsError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        msg = bfs_csr_status_string(status).decode()
+        super().__init__("%s: %s (status %d)" % (what, msg, status) if what else msg)
+
+
+def _check(status: int, what: str, handle=None):
+    if status != BFS_CSR_OK:
+        err = BfsError(status, what)
+        if handle is not None and status == BFS_CSR_ECUDA:
+            err.cuda_error = bfs_csr_last_cuda_error(handle)
+        raise err
+
+
+def default_options(**overrides) -> bfs_csr_options:
+    opt = bfs_csr_options()
+    _check(bfs_csr_default_options(ctypes.byref(opt)), "bfs_csr_default_options")
+    for k, v in overrides.items():
+        if not hasattr(opt, k):
+            raise AttributeError("bfs_csr_options has no field %r" % k)
+        setattr(opt, k, v)
+    return opt
+
+
+def workspace_bytes(n: int, nnz: int, row_ptr_64: bool, options=None) -> int:
+    out = _sz(0)
+    opt = ctypes.byref(options) if options is not None else None
+    _check(bfs_csr_workspace_bytes(n, nnz, int(row_ptr_64), opt, ctypes.byref(out)),
+           "bfs_csr_workspace_bytes")
+    return int(out.value)
+
+
+def _stream_ptr(stream) -> int | None:
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+class BfsCsr:
+    """A search handle over a device CSR held in torch tensors.
+
+    ``row_ptr`` (int32 or int64, n + 1) and ``col`` (int32, nnz) must be
+    contiguous CUDA tensors that outlive the handle. The workspace is a torch
+    uint8 tensor owned by this object.
+    """
+
+    def __init__(self, row_ptr, col, symmetric: bool = True, options=None, stream=None):
+        import torch
+        if not (row_ptr.is_cuda and col.is_cuda):
+            raise ValueError("row_ptr and col must be CUDA tensors")
+        if row_ptr.dtype not in (torch.int32, torch.int64) or col.dtype != torch.int32:
+            raise ValueError("row_ptr must be int32/int64 and col int32")
+        self.row_ptr = row_ptr.contiguous()
+        self.col = col.contiguous()
+        self.n = int(row_ptr.numel() - 1)
+        self.nnz = int(col.numel())
+        self.row_ptr_64 = row_ptr.dtype == torch.int64
+        self.symmetric = bool(symmetric)
+        self.options = options if options is not None else default_options()
+        nbytes = workspace_bytes(self.n, self.nnz, self.row_ptr_64, self.options)
+        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=row_ptr.device)
+        h = _vp()
+        status = bfs_csr_create(ctypes.byref(h), self.n, self.nnz, self.row_ptr.data_ptr(),
+                                int(self.row_ptr_64),
+                                self.col.data_ptr() if self.nnz else None,
+                                int(self.symmetric), self.workspace.data_ptr(), nbytes,
+                                ctypes.byref(self.options), _stream_ptr(stream))
+        _check(status, "bfs_csr_create")
+        self.handle = h
+
+    def run(self, source: int, dist, parent=None, num_levels=None, stream=None) -> None:
+        """Enqueue a search; results land in the given int32 CUDA tensors."""
+        status = bfs_csr_run(self.handle, int(source), dist.data_ptr(),
+                             parent.data_ptr() if parent is not None else None,
+                             num_levels.data_ptr() if num_levels is not None else None,
+                             _stream_ptr(stream))
+        _check(status, "bfs_csr_run", self.handle)
+
+    def run_init(self, source: int, dist, parent=None, stream=None) -> None:
+        """First half of :meth:`run`: reset and seed (one kernel)."""
+        status = bfs_csr_run_init(self.handle, int(source), dist.data_ptr(),
+                                  parent.data_ptr() if parent is not None else None,
+                                  _stream_ptr(stream))
+        _check(status, "bfs_csr_run_init", self.handle)
+
+    def run_levels(self, num_levels=None, stream=None) -> None:
+        """Second half of :meth:`run`: the level loop."""
+        status = bfs_csr_run_levels(self.handle,
+                                    num_levels.data_ptr() if num_levels is not None else None,
+                                    _stream_ptr(stream))
+        _check(status, "bfs_csr_run_levels", self.handle)
+
+    def sync(self, stream=None) -> int:
+        levels = ctypes.c_int32(0)
+        _check(bfs_csr_sync(self.handle, _stream_ptr(stream), ctypes.byref(levels)),
+               "bfs_csr_sync", self.handle)
+        return int(levels.value)
+
+    def search(self, source: int, want_parent: bool = True, stream=None):
+        """Run one search and wait: returns (dist, parent or None, num_levels)."""
+        import torch
+        dev = self.row_ptr.device
+        dist = torch.empty(self.n, dtype=torch.int32, device=dev)
+        parent = torch.empty(self.n, dtype=torch.int32, device=dev) if want_parent else None
+        self.run(source, dist, parent, stream=stream)
+        levels = self.sync(stream)
+        return dist, parent, levels
+
+    def level_stats(self):
+        cap = 1 << 16
+        buf = (bfs_csr_level_stat * cap)()
+        count = ctypes.c_int32(0)
+        _check(bfs_csr_level_stats(self.handle, buf, cap, ctypes.byref(count)),
+               "bfs_csr_level_stats")
+        out = []
+        for i in range(min(int(count.value), cap)):
+            s = buf[i]
+            out.append({"level": s.level, "direction": s.direction, "advance": s.advance,
+                        "frontier": s.frontier, "frontier_edges": s.frontier_edges,
+                        "unvisited": s.unvisited, "max_degree": s.max_degree,
+                        "t_start_ns": s.t_start_ns})
+        return out
+
+    def close(self) -> None:
+        if getattr(self, "handle", None):
+            bfs_csr_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class BfsCsrHost:
+    """A handle whose CSR and results live in host memory (numpy arrays).
+
+    The library keeps device copies; :meth:`run` optionally re-uploads the
+    CSR, searches, and copies dist/parent back before returning.
+    """
+
+    def __init__(self, row_ptr, col, symmetric: bool = True, options=None, stream=None):
+        import numpy as np
+        self.row_ptr = np.ascontiguousarray(row_ptr)
+        if self.row_ptr.dtype not in (np.int32, np.int64):
+            raise ValueError("row_ptr must be int32 or int64")
+        self.col = np.ascontiguousarray(col, dtype=np.int32)
+        self.n = int(self.row_ptr.shape[0] - 1)
+        self.nnz = int(self.col.shape[0])
+        self.row_ptr_64 = self.row_ptr.dtype == np.int64
+        self.options = options if options is not None else default_options()
+        h = _vp()
+        status = bfs_csr_create_host(ctypes.byref(h), self.n, self.nnz,
+                                     self.row_ptr.ctypes.data, int(self.row_ptr_64),
+                                     self.col.ctypes.data if self.nnz else None, int(symmetric),
+                                     ctypes.byref(self.options), _stream_ptr(stream))
+        _check(status, "bfs_csr_create_host")
+        self.handle = h
+
+    def run(self, source: int, dist, parent=None, row_ptr=None, col=None, stream=None) -> int:
+        levels = ctypes.c_int32(0)
+        status = bfs_csr_run_host(self.handle, int(source),
+                                  row_ptr.ctypes.data if row_ptr is not None else None,
+                                  col.ctypes.data if col is not None else None,
+                                  dist.ctypes.data,
+                                  parent.ctypes.data if parent is not None else None,
+                                  ctypes.addressof(levels), _stream_ptr(stream))
+        _check(status, "bfs_csr_run_host", self.handle)
+        return int(levels.value)
+
+    def close(self) -> None:
+        if getattr(self, "handle", None):
+            bfs_csr_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,610 @@
+// bfs_csr.cu -- the C-ABI library: handle, workspace, launches.
+//
+// The device work lives in bfs_device.cuh; this file validates arguments,
+// carves the workspace, sizes the cooperative grid and drives the level loop
+// either once per run (persistent mode) or once per level with a
+// device-to-host read of the loop state in between (host mode, the
+// structure of the host loop in "100 Days of GPU, Day 38").
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "bfs_csr.h"
+#include "bfs_device.cuh"
+
+using fbc::Ctl;
+using fbc::Params;
+
+namespace {
+
+constexpr int kStatsCap = 1 << 16;
+constexpr int kDefaultBlock = 512;
+
+struct Layout {
+    size_t ctl, visited, dead, fb0, fb1, qv0, qv1, qbeg0, qbeg1, qoff0, qoff1, stats, total;
+};
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+Layout make_layout(int64_t n, int row_ptr_64)
+{
+    Layout L;
+    const size_t words = (size_t)((n + 31) / 32);
+    const size_t R = row_ptr_64 ? 8 : 4;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off = align_up(off + bytes, 256);
+        return at;
+    };
+    L.ctl = take(sizeof(Ctl));
+    L.visited = take(words * 4);
+    L.dead = take(words * 4);
+    L.fb0 = take(words * 4);
+    L.fb1 = take(words * 4);
+    L.qv0 = take((size_t)n * 4);
+    L.qv1 = take((size_t)n * 4);
+    L.qbeg0 = take((size_t)n * R);
+    L.qbeg1 = take((size_t)n * R);
+    L.qoff0 = take((size_t)n * R);
+    L.qoff1 = take((size_t)n * R);
+    L.stats = take((size_t)kStatsCap * sizeof(bfs_csr_level_stat));
+    L.total = off;
+    return L;
+}
+
+}  // namespace
+
+struct bfs_csr_t {
+    int64_t n = 0, nnz = 0;
+    int row_ptr_64 = 0;
+    const void* row_ptr = nullptr;
+    const int32_t* col = nullptr;
+    int symmetric = 0;
+    bfs_csr_options opt{};
+    unsigned char* ws = nullptr;
+    size_t ws_bytes = 0;
+    bool own_ws = false;
+    Layout L{};
+    int words = 0;
+    int eb = 0;
+    int device = 0;
+    int sm_count = 0;
+    int block = kDefaultBlock;
+    int grid = 0;
+    size_t smem = 0;
+    int last_cuda_error = 0;
+    int last_status = BFS_CSR_OK;
+    int last_num_levels = 0;
+    // outputs of the last bfs_csr_run_init, consumed by bfs_csr_run_levels
+    int32_t pending_source = -1;
+    int32_t* pending_dist = nullptr;
+    int32_t* pending_parent = nullptr;
+    // host-memory variant
+    bool host_mode = false;
+    void* d_row_ptr_own = nullptr;
+    int32_t* d_col_own = nullptr;
+    int32_t* d_dist_own = nullptr;
+    int32_t* d_parent_own = nullptr;
+    int32_t* d_levels_own = nullptr;
+};
+
+namespace {
+
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+int cuda_fail(bfs_csr_t* h, cudaError_t e)
+{
+    if (h != nullptr)
+        h->last_cuda_error = (int)e;
+    return e == cudaErrorMemoryAllocation ? BFS_CSR_ENOMEM : BFS_CSR_ECUDA;
+}
+
+#define FBC_CUDA(h, call)                         \
+    do {                                          \
+        cudaError_t e_ = (call);                  \
+        if (e_ != cudaSuccess)                    \
+            return cuda_fail((h), e_);            \
+    } while (0)
+
+int check_options(const bfs_csr_options& o)
+{
+    if (o.direction < BFS_CSR_DIR_AUTO || o.direction > BFS_CSR_DIR_PULL) return BFS_CSR_EINVAL;
+    if (o.advance < BFS_CSR_ADV_AUTO || o.advance > BFS_CSR_ADV_MERGE_PATH) return BFS_CSR_EINVAL;
+    if (o.discovery < BFS_CSR_DISC_BITMAP || o.discovery > BFS_CSR_DISC_CAS) return BFS_CSR_EINVAL;
+    if (o.loop_mode < BFS_CSR_LOOP_PERSISTENT || o.loop_mode > BFS_CSR_LOOP_HOST) return BFS_CSR_EINVAL;
+    if (o.small_max_degree < 1 || o.cta_min_degree < o.small_max_degree) return BFS_CSR_EINVAL;
+    if (o.merge_path_min_frontier < 0 || o.binned_max_degree < 1) return BFS_CSR_EINVAL;
+    if (!(o.pull_ratio >= 0.0)) return BFS_CSR_EINVAL;
+    if (o.block_threads != 0 && (o.block_threads < 64 || o.block_threads > 512 || o.block_threads % 32))
+        return BFS_CSR_EINVAL;
+    if (o.grid_blocks < 0 || o.barrier_timeout_ns <= 0) return BFS_CSR_EINVAL;
+    return BFS_CSR_OK;
+}
+
+// Bits of the packed (count, edges) counter given to the edge total.
+int edge_bits(int64_t n, int64_t nnz, int row_ptr_64)
+{
+    if (!row_ptr_64)
+        return 32;
+    int vb = 1;
+    while (vb < 63 && (int64_t(1) << vb) <= n)
+        ++vb;
+    const int eb = 64 - vb;
+    if (eb >= 63 || nnz < (int64_t(1) << eb))
+        return eb;
+    return -1;
+}
+
+template <typename RowT>
+void* level_kernel_ptr() { return reinterpret_cast<void*>(&fbc::level_kernel<RowT>); }
+
+template <typename RowT>
+int configure_grid(bfs_csr_t* h)
+{
+    h->block = h->opt.block_threads ? h->opt.block_threads : kDefaultBlock;
+    h->smem = fbc::level_smem_bytes<RowT>(h->block);
+    FBC_CUDA(h, cudaFuncSetAttribute(fbc::level_kernel<RowT>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h->smem));
+    int per_sm = 0;
+    FBC_CUDA(h, cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fbc::level_kernel<RowT>,
+                                                              h->block, h->smem));
+    if (per_sm < 1)
+        return BFS_CSR_EUNSUPPORTED;
+    const int full = per_sm * h->sm_count;
+    h->grid = h->opt.grid_blocks ? (h->opt.grid_blocks < full ? h->opt.grid_blocks : full) : full;
+    return BFS_CSR_OK;
+}
+
+template <typename RowT>
+Params<RowT> make_params(bfs_csr_t* h, int32_t* d_dist, int32_t* d_parent, int32_t* d_levels)
+{
+    Params<RowT> p;
+    std::memset(&p, 0, sizeof(p));
+    unsigned char* w = h->ws;
+    p.row_ptr = static_cast<const RowT*>(h->row_ptr);
+    p.col = h->col;
+    p.n = (int32_t)h->n;
+    p.words = h->words;
+    p.dist = d_dist;
+    p.parent = d_parent;
+    p.visited = reinterpret_cast<uint32_t*>(w + h->L.visited);
+    p.fb[0] = reinterpret_cast<uint32_t*>(w + h->L.fb0);
+    p.fb[1] = reinterpret_cast<uint32_t*>(w + h->L.fb1);
+    p.qv[0] = reinterpret_cast<int32_t*>(w + h->L.qv0);
+    p.qv[1] = reinterpret_cast<int32_t*>(w + h->L.qv1);
+    p.qbeg[0] = reinterpret_cast<RowT*>(w + h->L.qbeg0);
+    p.qbeg[1] = reinterpret_cast<RowT*>(w + h->L.qbeg1);
+    p.qoff[0] = reinterpret_cast<RowT*>(w + h->L.qoff0);
+    p.qoff[1] = reinterpret_cast<RowT*>(w + h->L.qoff1);
+    p.ctl = reinterpret_cast<Ctl*>(w + h->L.ctl);
+    p.stats = reinterpret_cast<bfs_csr_level_stat*>(w + h->L.stats);
+    p.stats_cap = kStatsCap;
+    p.num_levels_out = d_levels;
+    p.eb = h->eb;
+    p.direction = h->opt.direction;
+    p.advance = h->opt.advance;
+    p.discovery = h->opt.discovery;
+    p.small_max = h->opt.small_max_degree;
+    p.cta_min = h->opt.cta_min_degree;
+    p.mp_min_frontier = h->opt.merge_path_min_frontier;
+    p.binned_max_deg = h->opt.binned_max_degree;
+    p.pull_ratio = h->opt.pull_ratio;
+    p.max_depth = h->opt.max_depth;
+    p.symmetric = h->symmetric;
+    p.level_budget = INT_MAX;
+    p.timeout_ns = h->opt.barrier_timeout_ns;
+    p.unreachable_barrier = h->opt.test_unreachable_barrier ? 1 : 0;
+    return p;
+}
+
+int init_grid(bfs_csr_t* h) { return h->sm_count * 8; }
+
+template <typename RowT>
+int prepare(bfs_csr_t* h, cudaStream_t s)
+{
+    unsigned char* w = h->ws;
+    Ctl* ctl = reinterpret_cast<Ctl*>(w + h->L.ctl);
+    FBC_CUDA(h, cudaMemsetAsync(ctl, 0, sizeof(Ctl), s));
+    const RowT* rp = static_cast<const RowT*>(h->row_ptr);
+    if (h->opt.validate) {
+        fbc::validate_kernel<RowT><<<init_grid(h), 256, 0, s>>>(rp, h->col, h->n, h->nnz,
+                                                                 &ctl->validate_flags);
+        FBC_CUDA(h, cudaGetLastError());
+        int flags = 0;
+        FBC_CUDA(h, cudaMemcpyAsync(&flags, &ctl->validate_flags, sizeof(int),
+                                    cudaMemcpyDeviceToHost, s));
+        FBC_CUDA(h, cudaStreamSynchronize(s));
+        if (flags != 0)
+            return BFS_CSR_EINVAL;
+    }
+    fbc::dead_kernel<RowT><<<init_grid(h), 256, 0, s>>>(
+        rp, (int32_t)h->n, h->words, reinterpret_cast<uint32_t*>(w + h->L.dead), &ctl->nonisolated);
+    FBC_CUDA(h, cudaGetLastError());
+    FBC_CUDA(h, cudaStreamSynchronize(s));
+    return configure_grid<RowT>(h);
+}
+
+template <typename RowT>
+int launch_init(bfs_csr_t* h, int32_t source, int32_t* d_dist, int32_t* d_parent, cudaStream_t s)
+{
+    Params<RowT> p = make_params<RowT>(h, d_dist, d_parent, nullptr);
+    const uint32_t* dead = reinterpret_cast<const uint32_t*>(h->ws + h->L.dead);
+    fbc::init_kernel<RowT><<<init_grid(h), 256, 0, s>>>(p, dead, source, h->symmetric ? 1 : 0);
+    FBC_CUDA(h, cudaGetLastError());
+    return BFS_CSR_OK;
+}
+
+template <typename RowT>
+int launch_levels(bfs_csr_t* h, int32_t* d_dist, int32_t* d_parent, int32_t* d_levels,
+                  cudaStream_t s)
+{
+    Params<RowT> p = make_params<RowT>(h, d_dist, d_parent, d_levels);
+    void* args[] = {&p};
+    if (h->opt.loop_mode == BFS_CSR_LOOP_PERSISTENT) {
+        FBC_CUDA(h, cudaLaunchCooperativeKernel(level_kernel_ptr<RowT>(), dim3(h->grid),
+                                                dim3(h->block), args, h->smem, s));
+        return BFS_CSR_OK;
+    }
+    // Host loop: one launch per level and a device->host read of the state.
+    Ctl* ctl = reinterpret_cast<Ctl*>(h->ws + h->L.ctl);
+    p.level_budget = 1;
+    for (;;) {
+        FBC_CUDA(h, cudaLaunchCooperativeKernel(level_kernel_ptr<RowT>(), dim3(h->grid),
+                                                dim3(h->block), args, h->smem, s));
+        int state[2] = {0, 0};  // status, done
+        FBC_CUDA(h, cudaMemcpyAsync(state, &ctl->status, sizeof(state), cudaMemcpyDeviceToHost, s));
+        FBC_CUDA(h, cudaStreamSynchronize(s));
+        if (state[0] != BFS_CSR_OK || state[1] != 0)
+            break;
+    }
+    return BFS_CSR_OK;
+}
+
+int create_common(bfs_csr_t* h, void* d_workspace, size_t workspace_bytes, cudaStream_t s)
+{
+    h->L = make_layout(h->n, h->row_ptr_64);
+    h->words = (int)((h->n + 31) / 32);
+    if (d_workspace != nullptr) {
+        if (workspace_bytes < h->L.total || (reinterpret_cast<uintptr_t>(d_workspace) & 255u))
+            return BFS_CSR_EINVAL;
+        h->ws = static_cast<unsigned char*>(d_workspace);
+        h->ws_bytes = workspace_bytes;
+        h->own_ws = false;
+    } else {
+        void* p = nullptr;
+        FBC_CUDA(h, cudaMalloc(&p, h->L.total));
+        h->ws = static_cast<unsigned char*>(p);
+        h->ws_bytes = h->L.total;
+        h->own_ws = true;
+    }
+    return h->row_ptr_64 ? prepare<int64_t>(h, s) : prepare<int32_t>(h, s);
+}
+
+int validate_shape(int64_t n, int64_t nnz, int row_ptr_64, const bfs_csr_options* opt)
+{
+    if (n < 1 || n >= (int64_t(1) << 31) || nnz < 0)
+        return BFS_CSR_EINVAL;
+    if (!row_ptr_64 && nnz >= (int64_t(1) << 31))
+        return BFS_CSR_EINVAL;
+    if (edge_bits(n, nnz, row_ptr_64) < 0)
+        return BFS_CSR_EUNSUPPORTED;
+    if (opt != nullptr)
+        return check_options(*opt);
+    return BFS_CSR_OK;
+}
+
+void release(bfs_csr_t* h)
+{
+    if (h == nullptr)
+        return;
+    if (h->own_ws && h->ws != nullptr)
+        cudaFree(h->ws);
+    if (h->d_row_ptr_own) cudaFree(h->d_row_ptr_own);
+    if (h->d_col_own) cudaFree(h->d_col_own);
+    if (h->d_dist_own) cudaFree(h->d_dist_own);
+    if (h->d_parent_own) cudaFree(h->d_parent_own);
+    if (h->d_levels_own) cudaFree(h->d_levels_own);
+    delete h;
+}
+
+int init_handle(bfs_csr_t* h, int64_t n, int64_t nnz, int row_ptr_64, int symmetric,
+                const bfs_csr_options* opt)
+{
+    h->n = n;
+    h->nnz = nnz;
+    h->row_ptr_64 = row_ptr_64 ? 1 : 0;
+    h->symmetric = symmetric ? 1 : 0;
+    if (opt != nullptr)
+        h->opt = *opt;
+    else
+        bfs_csr_default_options(&h->opt);
+    h->eb = edge_bits(n, nnz, h->row_ptr_64);
+    FBC_CUDA(h, cudaGetDevice(&h->device));
+    FBC_CUDA(h, cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, h->device));
+    int coop = 0;
+    FBC_CUDA(h, cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, h->device));
+    if (!coop)
+        return BFS_CSR_EUNSUPPORTED;
+    return BFS_CSR_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int bfs_csr_default_options(bfs_csr_options* o)
+{
+    if (o == nullptr)
+        return BFS_CSR_EINVAL;
+    std::memset(o, 0, sizeof(*o));
+    o->direction = BFS_CSR_DIR_AUTO;
+    o->advance = BFS_CSR_ADV_AUTO;
+    o->discovery = BFS_CSR_DISC_BITMAP;
+    o->loop_mode = BFS_CSR_LOOP_PERSISTENT;
+    o->small_max_degree = 32;
+    o->cta_min_degree = 256;
+    o->merge_path_min_frontier = 4096;
+    o->binned_max_degree = 8192;
+    o->pull_ratio = 1.0;
+    o->max_depth = -1;
+    o->validate = 1;
+    o->block_threads = 0;
+    o->grid_blocks = 0;
+    o->barrier_timeout_ns = 10ll * 1000 * 1000 * 1000;
+    o->test_unreachable_barrier = 0;
+    return BFS_CSR_OK;
+}
+
+int bfs_csr_workspace_bytes(int64_t n, int64_t nnz, int row_ptr_64, const bfs_csr_options* opt,
+                            size_t* bytes)
+{
+    if (bytes == nullptr)
+        return BFS_CSR_EINVAL;
+    const int rc = validate_shape(n, nnz, row_ptr_64, opt);
+    if (rc != BFS_CSR_OK)
+        return rc;
+    *bytes = make_layout(n, row_ptr_64).total;
+    return BFS_CSR_OK;
+}
+
+int bfs_csr_create(bfs_csr_handle* out, int64_t n, int64_t nnz, const void* d_row_ptr,
+                   int row_ptr_64, const int32_t* d_col, int symmetric, void* d_workspace,
+                   size_t workspace_bytes, const bfs_csr_options* opt, void* stream)
+{
+    if (out == nullptr)
+        return BFS_CSR_EINVAL;
+    *out = nullptr;
+    int rc = validate_shape(n, nnz, row_ptr_64, opt);
+    if (rc != BFS_CSR_OK)
+        return rc;
+    if (d_row_ptr == nullptr || (nnz > 0 && d_col == nullptr))
+        return BFS_CSR_EINVAL;
+    bfs_csr_t* h = new (std::nothrow) bfs_csr_t();
+    if (h == nullptr)
+        return BFS_CSR_ENOMEM;
+    rc = init_handle(h, n, nnz, row_ptr_64, symmetric, opt);
+    if (rc == BFS_CSR_OK) {
+        h->row_ptr = d_row_ptr;
+        h->col = d_col;
+        rc = create_common(h, d_workspace, workspace_bytes, as_stream(stream));
+    }
+    if (rc != BFS_CSR_OK) {
+        release(h);
+        return rc;
+    }
+    *out = h;
+    return BFS_CSR_OK;
+}
+
+int bfs_csr_run_init(bfs_csr_handle h, int64_t source, int32_t* d_dist, int32_t* d_parent,
+                     void* stream)
+{
+    if (h == nullptr || d_dist == nullptr || source < 0 || source >= h->n)
+        return BFS_CSR_EINVAL;
+    if (h->opt.direction == BFS_CSR_DIR_PULL && !h->symmetric)
+        return BFS_CSR_EUNSUPPORTED;
+    h->pending_source = -1;
+    const int rc = h->row_ptr_64
+                       ? launch_init<int64_t>(h, (int32_t)source, d_dist, d_parent, as_stream(stream))
+                       : launch_init<int32_t>(h, (int32_t)source, d_dist, d_parent, as_stream(stream));
+    if (rc == BFS_CSR_OK) {
+        h->pending_source = (int32_t)source;
+        h->pending_dist = d_dist;
+        h->pending_parent = d_parent;
+    }
+    h->last_status = rc;
+    return rc;
+}
+
+int bfs_csr_run_levels(bfs_csr_handle h, int32_t* d_num_levels, void* stream)
+{
+    if (h == nullptr || h->pending_source < 0)
+        return BFS_CSR_EINVAL;
+    const int rc = h->row_ptr_64
+                       ? launch_levels<int64_t>(h, h->pending_dist, h->pending_parent, d_num_levels,
+                                                as_stream(stream))
+                       : launch_levels<int32_t>(h, h->pending_dist, h->pending_parent, d_num_levels,
+                                                as_stream(stream));
+    h->pending_source = -1;
+    h->last_status = rc;
+    return rc;
+}
+
+int bfs_csr_run(bfs_csr_handle h, int64_t source, int32_t* d_dist, int32_t* d_parent,
+                int32_t* d_num_levels, void* stream)
+{
+    const int rc = bfs_csr_run_init(h, source, d_dist, d_parent, stream);
+    if (rc != BFS_CSR_OK)
+        return rc;
+    return bfs_csr_run_levels(h, d_num_levels, stream);
+}
+
+int bfs_csr_sync(bfs_csr_handle h, void* stream, int32_t* num_levels)
+{
+    if (h == nullptr)
+        return BFS_CSR_EINVAL;
+    cudaStream_t s = as_stream(stream);
+    FBC_CUDA(h, cudaStreamSynchronize(s));
+    FBC_CUDA(h, cudaGetLastError());
+    const Ctl* ctl = reinterpret_cast<const Ctl*>(h->ws + h->L.ctl);
+    int state[5] = {0, 0, 0, 0, 0};  // status, done, level, num_levels (+pad)
+    FBC_CUDA(h, cudaMemcpy(state, &ctl->status, 4 * sizeof(int), cudaMemcpyDeviceToHost));
+    h->last_status = state[0];
+    h->last_num_levels = state[3];
+    if (num_levels != nullptr)
+        *num_levels = state[3];
+    if (state[0] == BFS_CSR_OK && state[1] == 0)
+        return BFS_CSR_EDEVICE;  // the loop ended without reaching its end state
+    return state[0];
+}
+
+int bfs_csr_level_stats(bfs_csr_handle h, bfs_csr_level_stat* host_buf, int32_t cap,
+                        int32_t* count)
+{
+    if (h == nullptr || count == nullptr || cap < 0 || (cap > 0 && host_buf == nullptr))
+        return BFS_CSR_EINVAL;
+    *count = h->last_num_levels;
+    int take = h->last_num_levels < cap ? h->last_num_levels : cap;
+    if (take > kStatsCap)
+        take = kStatsCap;
+    if (take > 0)
+        FBC_CUDA(h, cudaMemcpy(host_buf, h->ws + h->L.stats,
+                               (size_t)take * sizeof(bfs_csr_level_stat), cudaMemcpyDeviceToHost));
+    return BFS_CSR_OK;
+}
+
+int bfs_csr_create_host(bfs_csr_handle* out, int64_t n, int64_t nnz, const void* h_row_ptr,
+                        int row_ptr_64, const int32_t* h_col, int symmetric,
+                        const bfs_csr_options* opt, void* stream)
+{
+    if (out == nullptr)
+        return BFS_CSR_EINVAL;
+    *out = nullptr;
+    int rc = validate_shape(n, nnz, row_ptr_64, opt);
+    if (rc != BFS_CSR_OK)
+        return rc;
+    if (h_row_ptr == nullptr || (nnz > 0 && h_col == nullptr))
+        return BFS_CSR_EINVAL;
+    bfs_csr_t* h = new (std::nothrow) bfs_csr_t();
+    if (h == nullptr)
+        return BFS_CSR_ENOMEM;
+    cudaStream_t s = as_stream(stream);
+    rc = init_handle(h, n, nnz, row_ptr_64, symmetric, opt);
+    const size_t rp_bytes = (size_t)(n + 1) * (row_ptr_64 ? 8 : 4);
+    const size_t col_bytes = (size_t)(nnz > 0 ? nnz : 1) * 4;
+    auto alloc = [&](void** p, size_t b) {
+        if (rc != BFS_CSR_OK)
+            return;
+        const cudaError_t e = cudaMalloc(p, b);
+        if (e != cudaSuccess)
+            rc = cuda_fail(h, e);
+    };
+    alloc(&h->d_row_ptr_own, rp_bytes);
+    alloc(reinterpret_cast<void**>(&h->d_col_own), col_bytes);
+    alloc(reinterpret_cast<void**>(&h->d_dist_own), (size_t)n * 4);
+    alloc(reinterpret_cast<void**>(&h->d_parent_own), (size_t)n * 4);
+    alloc(reinterpret_cast<void**>(&h->d_levels_own), 4);
+    if (rc == BFS_CSR_OK) {
+        cudaError_t e = cudaMemcpyAsync(h->d_row_ptr_own, h_row_ptr, rp_bytes,
+                                        cudaMemcpyHostToDevice, s);
+        if (e == cudaSuccess && nnz > 0)
+            e = cudaMemcpyAsync(h->d_col_own, h_col, (size_t)nnz * 4, cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess)
+            rc = cuda_fail(h, e);
+    }
+    if (rc == BFS_CSR_OK) {
+        h->host_mode = true;
+        h->row_ptr = h->d_row_ptr_own;
+        h->col = h->d_col_own;
+        rc = create_common(h, nullptr, 0, s);
+    }
+    if (rc != BFS_CSR_OK) {
+        release(h);
+        return rc;
+    }
+    *out = h;
+    return BFS_CSR_OK;
+}
+
+int bfs_csr_run_host(bfs_csr_handle h, int64_t source, const void* h_row_ptr, const int32_t* h_col,
+                     int32_t* h_dist, int32_t* h_parent, int32_t* h_num_levels, void* stream)
+{
+    if (h == nullptr || !h->host_mode || h_dist == nullptr || source < 0 || source >= h->n)
+        return BFS_CSR_EINVAL;
+    if (h_row_ptr == nullptr && h_col != nullptr)
+        return BFS_CSR_EINVAL;
+    if (h_row_ptr != nullptr && h->nnz > 0 && h_col == nullptr)
+        return BFS_CSR_EINVAL;
+    cudaStream_t s = as_stream(stream);
+    if (h_row_ptr != nullptr) {
+        const size_t rp_bytes = (size_t)(h->n + 1) * (h->row_ptr_64 ? 8 : 4);
+        FBC_CUDA(h, cudaMemcpyAsync(h->d_row_ptr_own, h_row_ptr, rp_bytes, cudaMemcpyHostToDevice, s));
+        if (h->nnz > 0)
+            FBC_CUDA(h, cudaMemcpyAsync(h->d_col_own, h_col, (size_t)h->nnz * 4,
+                                        cudaMemcpyHostToDevice, s));
+        if (h->opt.validate) {
+            Ctl* ctl = reinterpret_cast<Ctl*>(h->ws + h->L.ctl);
+            FBC_CUDA(h, cudaMemsetAsync(&ctl->validate_flags, 0, sizeof(int), s));
+            int flags = 0;
+            if (h->row_ptr_64)
+                fbc::validate_kernel<int64_t><<<init_grid(h), 256, 0, s>>>(
+                    static_cast<const int64_t*>(h->row_ptr), h->col, h->n, h->nnz, &ctl->validate_flags);
+            else
+                fbc::validate_kernel<int32_t><<<init_grid(h), 256, 0, s>>>(
+                    static_cast<const int32_t*>(h->row_ptr), h->col, h->n, h->nnz, &ctl->validate_flags);
+            FBC_CUDA(h, cudaGetLastError());
+            FBC_CUDA(h, cudaMemcpyAsync(&flags, &ctl->validate_flags, sizeof(int),
+                                        cudaMemcpyDeviceToHost, s));
+            FBC_CUDA(h, cudaStreamSynchronize(s));
+            if (flags != 0)
+                return BFS_CSR_EINVAL;
+        }
+    }
+    int rc = bfs_csr_run(h, source, h->d_dist_own, h_parent ? h->d_parent_own : nullptr,
+                         h->d_levels_own, stream);
+    if (rc != BFS_CSR_OK)
+        return rc;
+    FBC_CUDA(h, cudaMemcpyAsync(h_dist, h->d_dist_own, (size_t)h->n * 4, cudaMemcpyDeviceToHost, s));
+    if (h_parent != nullptr)
+        FBC_CUDA(h, cudaMemcpyAsync(h_parent, h->d_parent_own, (size_t)h->n * 4,
+                                    cudaMemcpyDeviceToHost, s));
+    int32_t levels = 0;
+    rc = bfs_csr_sync(h, stream, &levels);
+    if (h_num_levels != nullptr)
+        *h_num_levels = levels;
+    return rc;
+}
+
+int bfs_csr_destroy(bfs_csr_handle h)
+{
+    if (h == nullptr)
+        return BFS_CSR_EINVAL;
+    release(h);
+    return BFS_CSR_OK;
+}
+
+const char* bfs_csr_status_string(int status)
+{
+    switch (status) {
+    case BFS_CSR_OK: return "ok";
+    case BFS_CSR_EINVAL: return "invalid argument or malformed CSR";
+    case BFS_CSR_ENOMEM: return "out of memory";
+    case BFS_CSR_ECUDA: return "CUDA error";
+    case BFS_CSR_ETIMEOUT: return "a device-wide wait timed out";
+    case BFS_CSR_EUNSUPPORTED: return "unsupported option or size";
+    case BFS_CSR_EDEVICE: return "device-side check failed";
+    default: return "unknown status";
+    }
+}
+
+int bfs_csr_last_cuda_error(bfs_csr_handle h)
+{
+    return h == nullptr ? 0 : h->last_cuda_error;
+}
+
+}  // extern "C"

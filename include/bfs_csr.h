@@ -1,0 +1,191 @@
+/*
+ * bfs_csr.h -- level-synchronous frontier BFS over a CSR graph on one GPU.
+ *
+ * Given row_ptr/col, a vertex count and a source vertex, a run produces
+ *   dist[v]   = number of hops from the source to v, or -1 if v is unreached;
+ *   parent[v] = a BFS-tree parent of v: an in-neighbour u with
+ *               dist[u] = dist[v] - 1 (parent[source] = source, -1 if unreached).
+ * The problem statement (CSR in, per-vertex hop count out, -1 = not reached)
+ * is that of "100 Days of GPU, Day 38: Graph traversal on a GPU" (section
+ * "What a level-synchronous search actually launches") and of "The Frontier
+ * Model for Parallel Breadth-First Search" (ch. 22, section 22.1). The pages
+ * define no parent array; any in-neighbour one level closer is equally valid
+ * ("Gunrock: advance, filter, and the ragged-frontier problem", "Done when").
+ *
+ * All functions are C-ABI, thread-compatible (one handle must not be used by
+ * two host threads at once) and return a status code; none prints or exits.
+ * Device pointers are CUDA global-memory addresses of the current device.
+ * `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ */
+#ifndef FRONTIER_BFS_CSR_H
+#define FRONTIER_BFS_CSR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------------ status */
+#define BFS_CSR_OK 0
+#define BFS_CSR_EINVAL 1        /* bad argument or malformed CSR */
+#define BFS_CSR_ENOMEM 2        /* a device or host allocation failed */
+#define BFS_CSR_ECUDA 3         /* a CUDA call failed; see bfs_csr_last_cuda_error */
+#define BFS_CSR_ETIMEOUT 4      /* a bounded device-wide wait expired */
+#define BFS_CSR_EUNSUPPORTED 5  /* option or size the library cannot serve */
+#define BFS_CSR_EDEVICE 6       /* a device-side consistency check failed */
+
+/* ----------------------------------------------------------------- options */
+/* Direction of a level. Pull (bottom-up) scans unvisited vertices for a
+ * neighbour in the frontier bitmap; it needs in-edges, so it is only
+ * available for a symmetric CSR (PMPP ch. 15 notes, section 15.3 push/pull
+ * and section 15.7 direction-optimised BFS). */
+#define BFS_CSR_DIR_AUTO 0      /* pull when frontier edges > pull_ratio * unvisited */
+#define BFS_CSR_DIR_PUSH 1
+#define BFS_CSR_DIR_PULL 2      /* every level is bottom-up */
+
+/* Load balance of a top-down (push) level. */
+#define BFS_CSR_ADV_AUTO 0      /* merge-path when |F| >= merge_path_min_frontier
+                                   or the largest frontier degree >= binned_max_degree */
+#define BFS_CSR_ADV_BINNED 1    /* thread / warp / CTA per vertex by degree */
+#define BFS_CSR_ADV_MERGE_PATH 2 /* edge-balanced: degree prefix + search */
+
+/* How a top-down level decides who discovered a vertex. */
+#define BFS_CSR_DISC_BITMAP 0   /* atomicOr on a visited bitmap */
+#define BFS_CSR_DISC_CAS 1      /* atomicCAS on dist (-1 -> level + 1) */
+
+/* Where the level loop runs. */
+#define BFS_CSR_LOOP_PERSISTENT 0 /* one cooperative kernel runs every level */
+#define BFS_CSR_LOOP_HOST 1       /* one launch plus one device->host read per level */
+
+typedef struct bfs_csr_options {
+    int32_t direction;               /* BFS_CSR_DIR_*, default AUTO */
+    int32_t advance;                 /* BFS_CSR_ADV_*, default AUTO */
+    int32_t discovery;               /* BFS_CSR_DISC_*, default BITMAP */
+    int32_t loop_mode;               /* BFS_CSR_LOOP_*, default PERSISTENT */
+    int32_t small_max_degree;        /* binned: degree < this -> thread per vertex (32) */
+    int32_t cta_min_degree;          /* binned: degree >= this -> CTA per vertex (256) */
+    int32_t merge_path_min_frontier; /* auto advance threshold on |F| (4096) */
+    int32_t binned_max_degree;       /* auto advance threshold on max degree (8192) */
+    double pull_ratio;               /* auto direction: pull iff m_F > pull_ratio*|U| (1.0) */
+    int32_t max_depth;               /* label only vertices within this many hops; <0: all */
+    int32_t validate;                /* nonzero: check the CSR at create (O(nnz)) */
+    int32_t block_threads;           /* CTA size of the level kernel; 0 = default (512) */
+    int32_t grid_blocks;             /* CTAs of the level kernel; 0 = fill every SM */
+    int64_t barrier_timeout_ns;      /* limit of any device-wide wait (10 s) */
+    int32_t test_unreachable_barrier;/* diagnostics only: nonzero makes the first
+                                        device-wide barrier wait for one CTA more than
+                                        exists, so the run ends with BFS_CSR_ETIMEOUT */
+    int32_t reserved[7];             /* zero */
+} bfs_csr_options;
+
+/* Per-level record, kept when the run completes (see bfs_csr_level_stats). */
+typedef struct bfs_csr_level_stat {
+    int32_t level;           /* k: the frontier holds the vertices at distance k */
+    int32_t direction;       /* BFS_CSR_DIR_PUSH or BFS_CSR_DIR_PULL */
+    int32_t advance;         /* push levels: BFS_CSR_ADV_BINNED or _MERGE_PATH */
+    int32_t reserved;
+    int64_t frontier;        /* |F_k| */
+    int64_t frontier_edges;  /* m_F: sum of out-degrees over F_k */
+    int64_t unvisited;       /* non-isolated vertices not yet reached at level start */
+    int64_t max_degree;      /* largest out-degree in F_k */
+    int64_t t_start_ns;      /* device global timer at the level's start */
+} bfs_csr_level_stat;
+
+typedef struct bfs_csr_t *bfs_csr_handle;
+
+/* Fill *opt with the defaults listed above. */
+int bfs_csr_default_options(bfs_csr_options *opt);
+
+/* Bytes of device workspace a handle needs for a graph of n vertices and
+ * nnz entries (row_ptr of int64 when row_ptr_64 != 0). opt may be NULL. */
+int bfs_csr_workspace_bytes(int64_t n, int64_t nnz, int row_ptr_64,
+                            const bfs_csr_options *opt, size_t *bytes);
+
+/*
+ * Adopt a device CSR. d_row_ptr holds n + 1 offsets (int32, or int64 when
+ * row_ptr_64 != 0) with row_ptr[0] = 0 and row_ptr[n] = nnz; d_col holds nnz
+ * int32 vertex ids. Both are borrowed: they must stay unchanged and alive
+ * until bfs_csr_destroy. symmetric != 0 declares that the CSR is its own
+ * transpose (every u->v has v->u), which enables pull levels. d_workspace may
+ * be NULL (the library allocates and frees it) or caller memory of at least
+ * bfs_csr_workspace_bytes, 256-byte aligned, owned by the caller. With
+ * opt->validate the CSR is checked on the device; a malformed CSR gives
+ * BFS_CSR_EINVAL. Limits: 1 <= n < 2^31, nnz < 2^31 for int32 row_ptr.
+ * The call synchronises `stream`.
+ */
+int bfs_csr_create(bfs_csr_handle *out, int64_t n, int64_t nnz,
+                   const void *d_row_ptr, int row_ptr_64, const int32_t *d_col,
+                   int symmetric, void *d_workspace, size_t workspace_bytes,
+                   const bfs_csr_options *opt, void *stream);
+
+/*
+ * Enqueue one search from `source` on `stream`. d_dist (n int32, required),
+ * d_parent (n int32, may be NULL) and d_num_levels (one int32, may be NULL:
+ * the number of non-empty frontiers, i.e. the source's eccentricity + 1 when
+ * no depth bound cuts it short) are caller-owned device memory. The call is
+ * asynchronous in the persistent loop mode; in the host loop mode it
+ * synchronises `stream` once per level. Device-side failures (a wait that
+ * timed out) are reported by bfs_csr_sync. Returns BFS_CSR_EINVAL for a
+ * source outside [0, n) or a NULL d_dist, BFS_CSR_EUNSUPPORTED for forced
+ * pull on a non-symmetric graph.
+ */
+int bfs_csr_run(bfs_csr_handle h, int64_t source, int32_t *d_dist,
+                int32_t *d_parent, int32_t *d_num_levels, void *stream);
+
+/*
+ * The two halves of bfs_csr_run, for callers that time or schedule them
+ * separately: bfs_csr_run_init resets the run state and seeds `source`
+ * (dist/parent filled with -1, source with 0 / itself: one kernel);
+ * bfs_csr_run_levels then runs the level loop (one cooperative kernel, or
+ * one launch per level in the host loop mode) on the outputs given to the
+ * preceding bfs_csr_run_init of this handle. Same arguments, errors and
+ * asynchrony as bfs_csr_run; calling run_levels without a preceding
+ * run_init gives BFS_CSR_EINVAL.
+ */
+int bfs_csr_run_init(bfs_csr_handle h, int64_t source, int32_t *d_dist,
+                     int32_t *d_parent, void *stream);
+int bfs_csr_run_levels(bfs_csr_handle h, int32_t *d_num_levels, void *stream);
+
+/* Wait for the handle's last run on `stream`; return its device status and
+ * store the level count in *num_levels (may be NULL). */
+int bfs_csr_sync(bfs_csr_handle h, void *stream, int32_t *num_levels);
+
+/* Copy up to cap per-level records of the last synchronised run to host
+ * memory; *count receives the number of levels the run had. */
+int bfs_csr_level_stats(bfs_csr_handle h, bfs_csr_level_stat *host_buf,
+                        int32_t cap, int32_t *count);
+
+/*
+ * Host-memory variant for callers whose graph and results live on the host.
+ * bfs_csr_create_host allocates device copies of the CSR, the workspace and
+ * the outputs, uploads the CSR and validates it as bfs_csr_create does.
+ * bfs_csr_run_host then (1) re-uploads the CSR from h_row_ptr/h_col when they
+ * are non-NULL (same n and nnz; checked again when validation is on), (2)
+ * runs the search, (3) copies dist, parent (if h_parent != NULL) and the level
+ * count back, and synchronises `stream` before returning the run's status.
+ * Pinned host memory makes the copies asynchronous and fast.
+ */
+int bfs_csr_create_host(bfs_csr_handle *out, int64_t n, int64_t nnz,
+                        const void *h_row_ptr, int row_ptr_64,
+                        const int32_t *h_col, int symmetric,
+                        const bfs_csr_options *opt, void *stream);
+int bfs_csr_run_host(bfs_csr_handle h, int64_t source, const void *h_row_ptr,
+                     const int32_t *h_col, int32_t *h_dist, int32_t *h_parent,
+                     int32_t *h_num_levels, void *stream);
+
+/* Release everything the library allocated for the handle. */
+int bfs_csr_destroy(bfs_csr_handle h);
+
+/* Static text for a status code. */
+const char *bfs_csr_status_string(int status);
+
+/* The last CUDA error code recorded on the handle (0 if none). */
+int bfs_csr_last_cuda_error(bfs_csr_handle h);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FRONTIER_BFS_CSR_H */

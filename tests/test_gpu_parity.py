@@ -1,0 +1,312 @@
+"""GPU parity: the CUDA path through the C-ABI against the CPU oracle.
+
+dist must equal the oracle's bit for bit (BFS distances are unique); parent
+must be a valid BFS tree (checked by the oracle's checker, since several
+trees are correct); the level count and the per-level frontier sizes must
+equal the oracle's (the sizes summing to the reached count is the gate that
+catches a vertex queued twice, "100 Days of GPU, Day 38", "Pitfalls").
+"""
+import numpy as np
+import pytest
+
+import graphgen
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def fbc():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__._load_build_module().build()
+    import frontier_bfs_csr_gb300
+    return frontier_bfs_csr_gb300
+
+
+def _dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to("cuda")
+
+
+def check_against_oracle(fbc, g, sources, bfs=None, max_depth=-1, stats=True):
+    """Run each source on the GPU and compare with the oracle."""
+    own = bfs is None
+    if own:
+        bfs = fbc.BfsCsr(_dev(g.row_ptr), _dev(g.col), symmetric=g.symmetric)
+    for s in sources:
+        s = int(s)
+        dist, parent, levels = bfs.search(s)
+        dist_h = dist.cpu().numpy()
+        parent_h = parent.cpu().numpy()
+        want, _, want_levels = oracle.bfs(g.row_ptr, g.col, s, max_depth=max_depth,
+                                          want_parent=False)
+        if not np.array_equal(dist_h, want):
+            bad = np.nonzero(dist_h != want)[0]
+            raise AssertionError("%s source %d: dist differs at %d vertices, first %d "
+                                 "(gpu %d, oracle %d)" % (g.name, s, bad.size, bad[0],
+                                                          dist_h[bad[0]], want[bad[0]]))
+        assert levels == want_levels, (g.name, s, levels, want_levels)
+        code, where = oracle.check_parent(g.row_ptr, g.col, s, dist_h, parent_h)
+        assert code == 0, "%s source %d: invalid parent at %d" % (g.name, s, where)
+        if stats:
+            sizes, _, reached, _ = oracle.level_sizes(g.row_ptr, want)
+            rec = bfs.level_stats()
+            assert len(rec) == want_levels
+            got = [r["frontier"] for r in rec]
+            assert got == sizes.tolist(), (g.name, s)
+            assert sum(got) == reached
+    if own:
+        bfs.close()
+
+
+# ---------------------------------------------------------------- goldens
+
+def test_six_vertex_directed_golden(fbc, golden):
+    gx = golden("six_vertex_directed.json")
+    g = graphgen.from_csr(np.array(gx["row_ptr"], np.int32), np.array(gx["col"], np.int32),
+                          symmetric=False, name="six")
+    bfs = fbc.BfsCsr(_dev(g.row_ptr), _dev(g.col), symmetric=False)
+    dist, parent, levels = bfs.search(0)
+    assert dist.cpu().tolist() == gx["dist"]
+    assert levels == gx["num_levels"]
+    assert oracle.check_parent(g.row_ptr, g.col, 0, dist.cpu().numpy(), parent.cpu().numpy())[0] == 0
+    assert [r["frontier"] for r in bfs.level_stats()] == [len(f) for f in gx["levels"]]
+    bfs.close()
+    opt = fbc.default_options(max_depth=gx["after_level_1"]["max_depth"])
+    bfs = fbc.BfsCsr(_dev(g.row_ptr), _dev(g.col), symmetric=False, options=opt)
+    dist, _, levels = bfs.search(0)
+    assert dist.cpu().tolist() == gx["after_level_1"]["dist"] and levels == 3
+    bfs.close()
+
+
+def test_four_vertex_golden(fbc, golden):
+    gx = golden("four_vertex_undirected.json")
+    rp, col = np.array(gx["row_ptr"], np.int32), np.array(gx["col"], np.int32)
+    for direction in (fbc.BFS_CSR_DIR_PUSH, fbc.BFS_CSR_DIR_PULL, fbc.BFS_CSR_DIR_AUTO):
+        bfs = fbc.BfsCsr(_dev(rp), _dev(col), True, fbc.default_options(direction=direction))
+        for s, want in gx["dist_from"].items():
+            dist, parent, levels = bfs.search(int(s))
+            assert dist.cpu().tolist() == want and levels == max(want) + 1
+            assert oracle.check_parent(rp, col, int(s), dist.cpu().numpy(),
+                                       parent.cpu().numpy())[0] == 0
+        bfs.close()
+
+
+# ---------------------------------------------------------------- small graphs
+
+def test_random_small_graphs_every_source(fbc):
+    for k in range(120):
+        n = 1 + (k % 12)
+        directed = bool(k % 2)
+        g = graphgen.random_graph(n, [0.15, 0.3, 0.5][k % 3], 300 + k, directed=directed,
+                                  loops=directed and k % 3 == 0)
+        check_against_oracle(fbc, g, range(n))
+
+
+def test_corner_cases(fbc):
+    cases = [
+        (graphgen.from_edges(1, [], []), [0]),
+        (graphgen.from_edges(5, [], []), [0, 4]),
+        (graphgen.from_edges(6, [0, 3], [1, 4]), [0, 2, 3, 5]),
+        (graphgen.path_graph(2000), [0, 1000, 1999]),
+        (graphgen.star_graph(5000), [0, 17]),
+        (graphgen.clique_graph(64), [0, 63]),
+        (graphgen.grid(30, 50, 0.0, 0), [0, 777]),
+    ]
+    for g, srcs in cases:
+        check_against_oracle(fbc, g, srcs)
+
+
+def test_self_loops_and_duplicate_edges(fbc):
+    rng = np.random.default_rng(5)
+    src = rng.integers(0, 300, 3000)
+    dst = rng.integers(0, 300, 3000)
+    g = graphgen.from_edges(300, src, dst, symmetric=False, drop_loops=False, dedupe=False)
+    assert (np.repeat(np.arange(300), np.diff(g.row_ptr)) == g.col).any()
+    check_against_oracle(fbc, g, [0, 5, 299])
+    gs = graphgen.from_edges(300, np.concatenate([src, dst]), np.concatenate([dst, src]),
+                             symmetric=False, drop_loops=False, dedupe=False)
+    gs.symmetric = True  # every edge is present in both directions
+    check_against_oracle(fbc, gs, [0, 5, 299])
+
+
+def test_int64_row_ptr(fbc):
+    g = graphgen.rmat(12, 8, 11, row_ptr_64=True)
+    assert g.row_ptr.dtype == np.int64
+    check_against_oracle(fbc, g, graphgen.pick_sources(g, 6, 11))
+
+
+# ---------------------------------------------------------------- configs
+
+def test_config1_all_sources(fbc):
+    g = graphgen.config(1)
+    deg = g.degrees()
+    cand = np.nonzero(deg)[0]
+    ecc = [(oracle.bfs(g.row_ptr, g.col, int(s), want_parent=False)[2], int(s)) for s in cand]
+    best = max(ecc, key=lambda t: (t[0], -t[1]))[1]
+    check_against_oracle(fbc, g, [best] + list(g.sources))
+
+
+@pytest.mark.parametrize("cfg,count", [(2, 6), (3, 6), (4, 1)])
+def test_configs_2_to_4(fbc, cfg, count):
+    g = graphgen.config(cfg)
+    check_against_oracle(fbc, g, g.sources[:count])
+
+
+def test_config5_rmat25_sampled(fbc):
+    g = graphgen.config(5)
+    assert g.row_ptr.dtype == np.int64 and g.n == 1 << 25
+    bfs = fbc.BfsCsr(_dev(g.row_ptr), _dev(g.col), symmetric=True)
+    check_against_oracle(fbc, g, g.sources[:2], bfs=bfs)
+    # the remaining sources: distances certified by the invariant check
+    for s in g.sources[2:6]:
+        dist, parent, levels = bfs.search(int(s))
+        d = dist.cpu().numpy()
+        assert oracle.check_dist(g.row_ptr, g.col, int(s), d)[0] == 0
+        assert oracle.check_parent(g.row_ptr, g.col, int(s), d, parent.cpu().numpy())[0] == 0
+        assert levels == int(d.max()) + 1
+    bfs.close()
+
+
+# ---------------------------------------------------------------- option matrix
+
+OPTION_MATRIX = [
+    dict(direction=1, advance=1), dict(direction=1, advance=2), dict(direction=2),
+    dict(direction=0, advance=1), dict(direction=0, advance=2), dict(discovery=1),
+    dict(discovery=1, direction=1, advance=2), dict(loop_mode=1), dict(loop_mode=1, direction=1),
+    dict(block_threads=64), dict(block_threads=256, advance=2), dict(grid_blocks=1),
+    dict(grid_blocks=3, advance=1), dict(grid_blocks=7, advance=2, direction=1),
+    dict(small_max_degree=1, cta_min_degree=2, advance=1),
+    dict(small_max_degree=4, cta_min_degree=64, advance=1, direction=1),
+    dict(merge_path_min_frontier=0), dict(pull_ratio=0.0), dict(pull_ratio=100.0),
+]
+
+
+@pytest.mark.parametrize("over", OPTION_MATRIX, ids=lambda d: ",".join(
+    "%s=%s" % kv for kv in sorted(d.items())))
+def test_option_matrix(fbc, over):
+    opt = fbc.default_options(**over)
+    for cfg in (1, 3):
+        g = graphgen.config(cfg)
+        bfs = fbc.BfsCsr(_dev(g.row_ptr), _dev(g.col), True, opt)
+        check_against_oracle(fbc, g, g.sources[:3], bfs=bfs)
+        bfs.close()
+    g = graphgen.random_graph(11, 0.3, 42, directed=True)
+    if over.get("direction") != 2:
+        bfs = fbc.BfsCsr(_dev(g.row_ptr), _dev(g.col), False, opt)
+        check_against_oracle(fbc, g, range(11), bfs=bfs)
+        bfs.close()
+
+
+def test_stage_overflow_path(fbc):
+    """One CTA, binned advance: a level where 3,000 frontier vertices each
+    discover 20 new leaves overflows the shared-memory stage; the overflow
+    vertices must be appended, never dropped (the privatised queue of the
+    PMPP ch. 15 notes, section 15.6, drops them)."""
+    hub, mids, leaves = 0, np.arange(1, 3001), 20
+    src = [np.zeros(3000, np.int64)]
+    dst = [mids]
+    nxt = 3001
+    for m in mids:
+        src.append(np.full(leaves, m))
+        dst.append(np.arange(nxt, nxt + leaves))
+        nxt += leaves
+    g = graphgen.from_edges(nxt, np.concatenate(src), np.concatenate(dst))
+    for over in (dict(grid_blocks=1, advance=1), dict(grid_blocks=1, advance=2),
+                 dict(grid_blocks=2, direction=1, advance=1, small_max_degree=8,
+                      cta_min_degree=16)):
+        bfs = fbc.BfsCsr(_dev(g.row_ptr), _dev(g.col), True, fbc.default_options(**over))
+        check_against_oracle(fbc, g, [hub, 5], bfs=bfs)
+        bfs.close()
+
+
+# ---------------------------------------------------------------- API behaviour
+
+def test_errors(fbc):
+    g = graphgen.config(1)
+    bfs = fbc.BfsCsr(_dev(g.row_ptr), _dev(g.col), True)
+    dist = torch.empty(g.n, dtype=torch.int32, device="cuda")
+    for bad_src in (-1, g.n, g.n + 100):
+        with pytest.raises(fbc.BfsError) as e:
+            bfs.run(bad_src, dist)
+        assert e.value.status == fbc.BFS_CSR_EINVAL
+    bfs.close()
+    rp = g.row_ptr.copy()
+    rp[10], rp[11] = rp[11], rp[10] - 1  # non-monotone
+    with pytest.raises(fbc.BfsError) as e:
+        fbc.BfsCsr(_dev(rp), _dev(g.col), True)
+    assert e.value.status == fbc.BFS_CSR_EINVAL
+    col = g.col.copy()
+    col[7] = g.n  # out of range
+    with pytest.raises(fbc.BfsError) as e:
+        fbc.BfsCsr(_dev(g.row_ptr), _dev(col), True)
+    assert e.value.status == fbc.BFS_CSR_EINVAL
+    d = graphgen.random_graph(8, 0.4, 3, directed=True)
+    bfs = fbc.BfsCsr(_dev(d.row_ptr), _dev(d.col), False, fbc.default_options(direction=2))
+    with pytest.raises(fbc.BfsError) as e:
+        bfs.run(0, torch.empty(8, dtype=torch.int32, device="cuda"))
+    assert e.value.status == fbc.BFS_CSR_EUNSUPPORTED
+    bfs.close()
+
+
+def test_barrier_timeout_is_reported_and_recoverable(fbc):
+    """A barrier that waits for one CTA more than exists must give up after
+    the time limit, report BFS_CSR_ETIMEOUT, and leave the context usable."""
+    g = graphgen.config(1)
+    opt = fbc.default_options(test_unreachable_barrier=1, barrier_timeout_ns=50_000_000)
+    bfs = fbc.BfsCsr(_dev(g.row_ptr), _dev(g.col), True, opt)
+    dist = torch.empty(g.n, dtype=torch.int32, device="cuda")
+    bfs.run(int(g.sources[0]), dist)
+    with pytest.raises(fbc.BfsError) as e:
+        bfs.sync()
+    assert e.value.status == fbc.BFS_CSR_ETIMEOUT
+    bfs.close()
+    check_against_oracle(fbc, g, g.sources[:2])
+
+
+def test_output_without_parent_and_device_level_count(fbc):
+    g = graphgen.config(1)
+    bfs = fbc.BfsCsr(_dev(g.row_ptr), _dev(g.col), True)
+    s = int(g.sources[1])
+    dist = torch.empty(g.n, dtype=torch.int32, device="cuda")
+    nl = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bfs.run(s, dist, None, nl)
+    levels = bfs.sync()
+    want, _, want_levels = oracle.bfs(g.row_ptr, g.col, s, want_parent=False)
+    assert np.array_equal(dist.cpu().numpy(), want)
+    assert levels == want_levels == int(nl.item())
+    bfs.close()
+
+
+def test_caller_workspace_and_streams(fbc):
+    g = graphgen.config(1)
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        bfs = fbc.BfsCsr(_dev(g.row_ptr), _dev(g.col), True, stream=stream)
+        outs = []
+        for s in g.sources[:4]:
+            dist = torch.empty(g.n, dtype=torch.int32, device="cuda")
+            bfs.run(int(s), dist, stream=stream)
+            bfs.sync(stream)
+            outs.append(dist.cpu().numpy())
+    for s, d in zip(g.sources[:4], outs):
+        assert np.array_equal(d, oracle.bfs(g.row_ptr, g.col, int(s), want_parent=False)[0])
+    bfs.close()
+
+
+def test_host_memory_api(fbc):
+    g = graphgen.config(1)
+    h = fbc.BfsCsrHost(g.row_ptr, g.col, True)
+    for s in g.sources[:4]:
+        dist = np.empty(g.n, np.int32)
+        parent = np.empty(g.n, np.int32)
+        levels = h.run(int(s), dist, parent, row_ptr=g.row_ptr, col=g.col)
+        want, _, want_levels = oracle.bfs(g.row_ptr, g.col, int(s), want_parent=False)
+        assert np.array_equal(dist, want) and levels == want_levels
+        assert oracle.check_parent(g.row_ptr, g.col, int(s), dist, parent)[0] == 0
+        levels = h.run(int(s), dist)  # resident CSR, no parent
+        assert np.array_equal(dist, want) and levels == want_levels
+    h.close()
