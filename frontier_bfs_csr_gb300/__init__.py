@@ -44,7 +44,9 @@ EXPORTED = [
     "bfs_csr_run_init", "bfs_csr_run_levels",
     "bfs_csr_sync", "bfs_csr_level_stats", "bfs_csr_create_host", "bfs_csr_run_host",
     "bfs_csr_destroy", "bfs_csr_status_string", "bfs_csr_last_cuda_error",
+    "bfs_csr_run_noalloc",
 ]
+BFS_CSR_NOALLOC_MAX_VERTICES = 1048576
 
 
 class bfs_csr_options(ctypes.Structure):
@@ -101,6 +103,8 @@ _sig = {
     "bfs_csr_destroy": ([_vp], _i32),
     "bfs_csr_status_string": ([_i32], ctypes.c_char_p),
     "bfs_csr_last_cuda_error": ([_vp], _i32),
+    "bfs_csr_run_noalloc": ([_i64, _i64, _vp, _vp, _i32, _i64, _vp, _vp, _vp,
+                             ctypes.POINTER(ctypes.c_int32), _opt_p, _vp], _i32),
 }
 for _name, (_args, _res) in _sig.items():
     _f = getattr(_lib, _name)

@@ -7,6 +7,7 @@
 // structure of the host loop in "100 Days of GPU, Day 38").
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <climits>
 #include <cstdint>
 #include <cstdlib>
@@ -608,3 +609,90 @@ int bfs_csr_last_cuda_error(bfs_csr_handle h)
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// The allocation-free variant. Its scratch is one device array of the library
+// itself, laid out exactly like a handle's workspace for the largest graph it
+// accepts; the host side keeps nothing but that array's per-device address.
+
+namespace {
+
+constexpr int64_t kNoAllocMaxN = BFS_CSR_NOALLOC_MAX_VERTICES;
+
+// Upper bound of make_layout(kNoAllocMaxN, 0).total: every region rounded up
+// to 256 bytes.
+constexpr size_t kNoAllocBytes =
+    (sizeof(Ctl) + 256) + 4 * ((size_t)kNoAllocMaxN / 8 + 256) +
+    2 * ((size_t)kNoAllocMaxN * 4 + 256) + 4 * ((size_t)kNoAllocMaxN * 4 + 256) +
+    ((size_t)kStatsCap * sizeof(bfs_csr_level_stat) + 256);
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+constexpr int kNoAllocMaxDevices = 64;
+std::atomic<void*> g_noalloc_addr[kNoAllocMaxDevices];
+
+// Device address of the scratch array on the current device (looked up once
+// per device; a host-side stand-in is never passed to a kernel).
+int noalloc_scratch(int device, void** out)
+{
+    if (device < 0 || device >= kNoAllocMaxDevices)
+        return BFS_CSR_EUNSUPPORTED;
+    void* p = g_noalloc_addr[device].load(std::memory_order_acquire);
+    if (p == nullptr) {
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || p == nullptr)
+            return BFS_CSR_ECUDA;
+        g_noalloc_addr[device].store(p, std::memory_order_release);
+    }
+    *out = p;
+    return BFS_CSR_OK;
+}
+
+}  // namespace
+
+extern "C" int bfs_csr_run_noalloc(int64_t n, int64_t nnz, const int32_t* d_row_ptr,
+                                   const int32_t* d_col, int symmetric, int64_t source,
+                                   int32_t* d_dist, int32_t* d_parent, int32_t* d_num_levels,
+                                   int32_t* num_levels, const bfs_csr_options* opt, void* stream)
+{
+    if (n > kNoAllocMaxN)
+        return BFS_CSR_EUNSUPPORTED;
+    int rc = validate_shape(n, nnz, 0, opt);
+    if (rc != BFS_CSR_OK)
+        return rc;
+    if (d_row_ptr == nullptr || (nnz > 0 && d_col == nullptr) || d_dist == nullptr ||
+        source < 0 || source >= n)
+        return BFS_CSR_EINVAL;
+    bfs_csr_t h;  // on the stack: nothing is allocated
+    rc = init_handle(&h, n, nnz, 0, symmetric, opt);
+    if (rc != BFS_CSR_OK)
+        return rc;
+    if (h.opt.direction == BFS_CSR_DIR_PULL && !h.symmetric)
+        return BFS_CSR_EUNSUPPORTED;
+    void* scratch = nullptr;
+    rc = noalloc_scratch(h.device, &scratch);
+    if (rc != BFS_CSR_OK)
+        return rc;
+    h.row_ptr = d_row_ptr;
+    h.col = d_col;
+    h.L = make_layout(n, 0);
+    if (h.L.total > kNoAllocBytes)
+        return BFS_CSR_EUNSUPPORTED;
+    h.words = (int)((n + 31) / 32);
+    h.ws = static_cast<unsigned char*>(scratch);
+    h.ws_bytes = kNoAllocBytes;
+    h.own_ws = false;
+    cudaStream_t s = as_stream(stream);
+    rc = prepare<int32_t>(&h, s);  // clears the control block, validates, dead bitmap
+    if (rc == BFS_CSR_OK)
+        rc = launch_init<int32_t>(&h, (int32_t)source, d_dist, d_parent, s);
+    if (rc == BFS_CSR_OK)
+        rc = launch_levels<int32_t>(&h, d_dist, d_parent, d_num_levels, s);
+    if (rc != BFS_CSR_OK)
+        return rc;
+    int32_t levels = 0;
+    rc = bfs_csr_sync(&h, stream, &levels);
+    if (num_levels != nullptr)
+        *num_levels = levels;
+    return rc;
+}

@@ -184,6 +184,42 @@ const char *bfs_csr_status_string(int status);
 /* The last CUDA error code recorded on the handle (0 if none). */
 int bfs_csr_last_cuda_error(bfs_csr_handle h);
 
+/*
+ * A search that allocates nothing, for callers that cannot call cudaMalloc:
+ * for example a process whose device memory already belongs to another
+ * allocator (a framework's caching pool that reserved the device), or a
+ * latency-critical path where the implicit synchronisation of
+ * cudaMalloc/cudaFree is not allowed. The pages have no counterpart; this is
+ * a deployment variant of bfs_csr_run.
+ *
+ * Instead of a handle and a workspace it uses one scratch array that lives
+ * in the library's own device memory (a file-scope __device__ array, about
+ * 28 MB, held on every GPU that loads the library until the process exits).
+ * That bounds the graph: n <= 1,048,576 vertices and an int32 row_ptr
+ * (nnz < 2^31); larger inputs are rejected with BFS_CSR_EUNSUPPORTED before
+ * any work. The caller still provides the device CSR (d_row_ptr: n + 1
+ * int32, d_col: nnz int32), d_dist (n int32, required), d_parent (n int32,
+ * may be NULL) and d_num_levels (one int32 on the device, may be NULL).
+ * opt may be NULL (defaults). No cudaMalloc, cudaFree or other allocating
+ * call is made, on the host or the device.
+ *
+ * The call runs synchronously on `stream`: it validates the CSR when
+ * opt->validate is set, searches, waits for the stream and returns the
+ * search's status (*num_levels, when not NULL, receives the level count on
+ * the host). The first call on a device looks up the scratch array's device
+ * address (cudaGetSymbolAddress) with that device current; make that first
+ * call before any stream capture. Every call shares the one scratch array
+ * and resets the parts that must start from zero; calls that overlap on the
+ * GPU (from two host threads or two streams) race on it and must not be
+ * issued.
+ */
+#define BFS_CSR_NOALLOC_MAX_VERTICES 1048576
+int bfs_csr_run_noalloc(int64_t n, int64_t nnz, const int32_t *d_row_ptr,
+                        const int32_t *d_col, int symmetric, int64_t source,
+                        int32_t *d_dist, int32_t *d_parent,
+                        int32_t *d_num_levels, int32_t *num_levels,
+                        const bfs_csr_options *opt, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
