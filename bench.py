@@ -256,7 +256,8 @@ def run_ours(args):
     barrier(torch, ws)
     if rank != 0:
         g = graphgen.config(args.config)
-    sources = rank_sources(g.sources, rank, ws)
+    all_sources = g.sources[:args.sources] if args.sources > 0 else g.sources
+    sources = rank_sources(all_sources, rank, ws)
     row_ptr = torch.from_numpy(g.row_ptr).to(device)
     col = torch.from_numpy(g.col).to(device)
     R = 8 if g.row_ptr_64 else 4
@@ -280,6 +281,7 @@ def run_ours(args):
         stats = bfs.level_stats()
         lb, per_level = algorithmic_bytes(torch, row_ptr.to(torch.int64), col, deg, src_of_edge,
                                           dist, stats, R)
+        torch.cuda.empty_cache()
         per_source[s] = {"levels": levels, "edges": edges, "level_bytes": lb,
                          "directions": "".join("P" if x["direction"] == DIR_PUSH else "U"
                                                for x in stats),
@@ -496,7 +498,7 @@ def run_reference(args):
     import oracle
     g = graphgen.config(args.config)
     deg = np.diff(g.row_ptr.astype(np.int64))
-    sources = [int(s) for s in g.sources]
+    sources = [int(s) for s in (g.sources[:args.sources] if args.sources > 0 else g.sources)]
     for i in range(args.warmup):
         oracle.bfs(g.row_ptr, g.col, sources[i % len(sources)])
     edges, elapsed = 0, 0.0
@@ -532,6 +534,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-overhead", action="store_true")
+    ap.add_argument("--sources", type=int, default=0,
+                    help="use only the first S sources of the workload (0: all)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

@@ -35,7 +35,7 @@ BFS_CSR_EUNSUPPORTED = 5
 BFS_CSR_EDEVICE = 6
 
 BFS_CSR_DIR_AUTO, BFS_CSR_DIR_PUSH, BFS_CSR_DIR_PULL = 0, 1, 2
-BFS_CSR_ADV_AUTO, BFS_CSR_ADV_BINNED, BFS_CSR_ADV_MERGE_PATH = 0, 1, 2
+BFS_CSR_ADV_AUTO, BFS_CSR_ADV_BINNED, BFS_CSR_ADV_MERGE_PATH, BFS_CSR_ADV_SINGLE_CTA = 0, 1, 2, 3
 BFS_CSR_DISC_BITMAP, BFS_CSR_DISC_CAS = 0, 1
 BFS_CSR_LOOP_PERSISTENT, BFS_CSR_LOOP_HOST = 0, 1
 
@@ -66,7 +66,8 @@ class bfs_csr_options(ctypes.Structure):
         ("grid_blocks", ctypes.c_int32),
         ("barrier_timeout_ns", ctypes.c_int64),
         ("test_unreachable_barrier", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 7),
+        ("narrow_max_edges", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 6),
     ]
 
 

@@ -123,7 +123,8 @@ int check_options(const bfs_csr_options& o)
     if (!(o.pull_ratio >= 0.0)) return BFS_CSR_EINVAL;
     if (o.block_threads != 0 && (o.block_threads < 64 || o.block_threads > 512 || o.block_threads % 32))
         return BFS_CSR_EINVAL;
-    if (o.grid_blocks < 0 || o.barrier_timeout_ns <= 0) return BFS_CSR_EINVAL;
+    if (o.grid_blocks < 0 || o.barrier_timeout_ns <= 0 || o.narrow_max_edges < 0)
+        return BFS_CSR_EINVAL;
     return BFS_CSR_OK;
 }
 
@@ -200,6 +201,10 @@ Params<RowT> make_params(bfs_csr_t* h, int32_t* d_dist, int32_t* d_parent, int32
     p.level_budget = INT_MAX;
     p.timeout_ns = h->opt.barrier_timeout_ns;
     p.unreachable_barrier = h->opt.test_unreachable_barrier ? 1 : 0;
+    {
+        const int cap = h->block * fbc::kItems;
+        p.narrow_max = h->opt.narrow_max_edges < cap ? h->opt.narrow_max_edges : cap;
+    }
     return p;
 }
 
@@ -358,6 +363,7 @@ int bfs_csr_default_options(bfs_csr_options* o)
     o->grid_blocks = 0;
     o->barrier_timeout_ns = 10ll * 1000 * 1000 * 1000;
     o->test_unreachable_barrier = 0;
+    o->narrow_max_edges = 2048;
     return BFS_CSR_OK;
 }
 

@@ -35,6 +35,7 @@
 // edge order agree and qoff[] is a valid exclusive scan of the degrees.
 #pragma once
 
+#include <climits>
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -59,6 +60,8 @@ struct __align__(16) LevelSlot {
     long long unvisited;        // U_k: non-isolated vertices unreached at level k
     int dir;                    // direction used at level k
     int adv;                    // advance used at level k (push levels)
+    unsigned int work_next;     // next chunk of level k handed out to a warp
+    unsigned int pad_slot;
 };
 
 struct __align__(128) Ctl {
@@ -69,7 +72,8 @@ struct __align__(128) Ctl {
     int done;                   // the search has ended
     int level;                  // next level to run (persists across launches)
     int num_levels;             // non-empty frontiers, valid once done
-    int pad1[27];
+    int solo_resume;            // first level after a single-CTA session
+    int pad1[26];
     LevelSlot slot[kSlots];
     unsigned long long t_end_ns;
     long long nonisolated;      // vertices of nonzero degree (set at create)
@@ -103,6 +107,7 @@ struct Params {
     int level_budget;           // levels this launch may run
     long long timeout_ns;
     int unreachable_barrier;
+    int narrow_max;             // single-CTA levels: frontier edges (and vertices) <= this
 };
 
 // ------------------------------------------------------------ primitives
@@ -131,11 +136,18 @@ __device__ __forceinline__ unsigned long long ldcg_u64(const unsigned long long*
     return __ldcg(p);
 }
 
+__device__ __forceinline__ void red_release_add_u64(unsigned long long* p, unsigned long long v)
+{
+    asm volatile("red.release.gpu.global.add.u64 [%0], %1;" :: "l"(p), "l"(v) : "memory");
+}
+
 // Grid-wide barrier with a bounded wait. All CTAs of the cooperative launch
-// call it the same number of times. Thread 0 publishes the CTA's writes
-// (fence), arrives, and polls the arrival counter with acquire loads until
-// every CTA has arrived or the time limit passes; on expiry it records
-// BFS_CSR_ETIMEOUT. Returns false when the run must stop.
+// call it the same number of times. After the CTA's own barrier, thread 0
+// arrives with a release add (publishing every write the CTA made before the
+// barrier) and polls the arrival counter with acquire loads until every CTA
+// has arrived or the time limit passes; on expiry it records
+// BFS_CSR_ETIMEOUT and the caller stops. A status set by another CTA is
+// picked up at the next level start.
 template <typename RowT>
 __device__ __forceinline__ bool grid_barrier(const Params<RowT>& p, unsigned long long& target)
 {
@@ -144,23 +156,20 @@ __device__ __forceinline__ bool grid_barrier(const Params<RowT>& p, unsigned lon
     if (threadIdx.x == 0) {
         target += gridDim.x;
         const unsigned long long want = target + (unsigned long long)p.unreachable_barrier;
-        __threadfence();
-        atomicAdd(&p.ctl->bar, 1ull);
-        const unsigned long long t0 = global_timer_ns();
-        unsigned int spins = 0;
+        red_release_add_u64(&p.ctl->bar, 1ull);
         int ok = 1;
-        while (ld_acquire_u64(&p.ctl->bar) < want) {
-            if ((++spins & 255u) == 0u) {
-                if (global_timer_ns() - t0 > (unsigned long long)p.timeout_ns || spins > (1u << 30)) {
+        if (ld_acquire_u64(&p.ctl->bar) < want) {
+            const unsigned long long t0 = global_timer_ns();
+            unsigned int spins = 0;
+            while (ld_acquire_u64(&p.ctl->bar) < want) {
+                if ((++spins & 63u) == 0u &&
+                    (global_timer_ns() - t0 > (unsigned long long)p.timeout_ns || spins > (1u << 30))) {
                     atomicCAS(&p.ctl->status, BFS_CSR_OK, BFS_CSR_ETIMEOUT);
                     ok = 0;
                     break;
                 }
             }
         }
-        __threadfence();
-        if (ok && ldcg(&p.ctl->status) != BFS_CSR_OK)
-            ok = 0;
         s_ok = ok;
     }
     __syncthreads();
@@ -253,6 +262,7 @@ struct __align__(16) SmemScalars {
     int i0;
     unsigned long long base;
     unsigned long long ebase;
+    unsigned long long solo_found, solo_edges, solo_maxdeg;
     long long tmp_ll[33];
 };
 
@@ -268,7 +278,7 @@ struct Tally {
 // Append one discovered vertex (degree > 0) to the next queue directly with a
 // single packed atomic. Used only when the shared-memory stage is full.
 template <typename RowT>
-__device__ __noinline__ void append_direct(const Params<RowT>& p, LevelSlot* nxt, int qsel,
+__device__ void append_direct(const Params<RowT>& p, LevelSlot* nxt, int qsel,
                                            int32_t v, RowT b, RowT deg)
 {
     const unsigned long long old = atomicAdd(&nxt->qpack, (1ull << p.eb) | (unsigned long long)deg);
@@ -367,10 +377,11 @@ __device__ void publish_tally(const Tally& t, LevelSlot* nxt, SmemScalars& ss)
 // The claim of vertex v by frontier vertex u at level k. Exactly one caller
 // per v gets true; the winner writes dist[v] and parent[v].
 template <typename RowT>
-__device__ __forceinline__ bool claim(const Params<RowT>& p, int k, int32_t v, int32_t u)
+__device__ __forceinline__ bool claim(const Params<RowT>& p, int k, int32_t v, int32_t u,
+                                      bool precheck)
 {
     if (p.discovery == BFS_CSR_DISC_CAS) {
-        if (ldcg(&p.dist[v]) != -1)
+        if (precheck && ldcg(&p.dist[v]) != -1)
             return false;
         if (atomicCAS(&p.dist[v], -1, k + 1) != -1)
             return false;
@@ -378,7 +389,7 @@ __device__ __forceinline__ bool claim(const Params<RowT>& p, int k, int32_t v, i
     } else {
         const uint32_t bit = 1u << (v & 31);
         uint32_t* w = p.visited + (v >> 5);
-        if (ldcg(w) & bit)
+        if (precheck && (ldcg(w) & bit))
             return false;
         if (atomicOr(w, bit) & bit)
             return false;
@@ -387,6 +398,53 @@ __device__ __forceinline__ bool claim(const Params<RowT>& p, int k, int32_t v, i
     if (p.parent != nullptr)
         p.parent[v] = u;
     return true;
+}
+
+// N claims at once: every load and atomic of the batch is issued before any
+// result is used, so their round trips overlap. v[i] < 0 marks an empty lane
+// of the batch.
+template <typename RowT, int N>
+__device__ __forceinline__ void claim_batch(const Params<RowT>& p, int k, const int32_t (&v)[N],
+                                            const int32_t (&u)[N], bool precheck, bool (&won)[N])
+{
+    if (p.discovery == BFS_CSR_DISC_CAS) {
+        int32_t seen[N];
+#pragma unroll
+        for (int i = 0; i < N; ++i)
+            seen[i] = (v[i] >= 0 && precheck) ? ldcg(&p.dist[v[i]]) : -1;
+#pragma unroll
+        for (int i = 0; i < N; ++i)
+            won[i] = v[i] >= 0 && seen[i] == -1 && atomicCAS(&p.dist[v[i]], -1, k + 1) == -1;
+#pragma unroll
+        for (int i = 0; i < N; ++i)
+            if (won[i])
+                atomicOr(&p.visited[v[i] >> 5], 1u << (v[i] & 31));
+    } else {
+        uint32_t seen[N];
+#pragma unroll
+        for (int i = 0; i < N; ++i)
+            seen[i] = (v[i] >= 0 && precheck) ? ldcg(p.visited + (v[i] >> 5)) : 0u;
+        uint32_t old[N];
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            const uint32_t bit = 1u << (v[i] & 31);
+            old[i] = bit;
+            if (v[i] >= 0 && !(seen[i] & bit))
+                old[i] = atomicOr(p.visited + (v[i] >> 5), bit);
+        }
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            won[i] = v[i] >= 0 && !(old[i] & (1u << (v[i] & 31)));
+            if (won[i])
+                p.dist[v[i]] = k + 1;
+        }
+    }
+    if (p.parent != nullptr) {
+#pragma unroll
+        for (int i = 0; i < N; ++i)
+            if (won[i])
+                p.parent[v[i]] = u[i];
+    }
 }
 
 // After a win: read v's row, count it, and queue it when it has edges.
@@ -404,6 +462,36 @@ __device__ __forceinline__ void after_win(const Params<RowT>& p, const Smem<RowT
         stage_push(p, sm, ss, nxt, qsel, v, b, deg);
 }
 
+// after_win for a batch: the row offsets of all winners are loaded together.
+template <typename RowT, int N>
+__device__ __forceinline__ void after_win_batch(const Params<RowT>& p, const Smem<RowT>& sm,
+                                                SmemScalars& ss, LevelSlot* nxt, int qsel,
+                                                Tally& t, const int32_t (&v)[N],
+                                                const bool (&won)[N])
+{
+    RowT b[N], e[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        b[i] = 0;
+        e[i] = 0;
+        if (won[i]) {
+            b[i] = p.row_ptr[v[i]];
+            e[i] = p.row_ptr[v[i] + 1];
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        if (!won[i])
+            continue;
+        const RowT deg = e[i] - b[i];
+        t.found += 1;
+        t.edges += (unsigned long long)deg;
+        t.maxdeg = (unsigned long long)deg > t.maxdeg ? (unsigned long long)deg : t.maxdeg;
+        if (deg > 0)
+            stage_push(p, sm, ss, nxt, qsel, v[i], b[i], deg);
+    }
+}
+
 // ------------------------------------------------------------ S4 push levels
 
 // Degree-binned advance: thread per vertex below small_max, warp per vertex
@@ -411,7 +499,7 @@ __device__ __forceinline__ void after_win(const Params<RowT>& p, const Smem<RowT
 // CTA i % G so that small frontiers spread over every SM.
 template <typename RowT>
 __device__ void push_binned(const Params<RowT>& p, int k, int qn, RowT qm, const Smem<RowT>& sm,
-                            SmemScalars& ss, LevelSlot* nxt, Tally& t)
+                            SmemScalars& ss, LevelSlot* nxt, Tally& t, bool pre)
 {
     const int cs = k & 1, ns = cs ^ 1;
     const int32_t* qv = p.qv[cs];
@@ -433,18 +521,16 @@ __device__ void push_binned(const Params<RowT>& p, int k, int qn, RowT qm, const
         }
         // thread per vertex
         if (valid && deg < (RowT)p.small_max) {
-            RowT j = 0;
-            for (; j + 4 <= deg; j += 4) {
-                const int32_t v0 = p.col[b + j], v1 = p.col[b + j + 1];
-                const int32_t v2 = p.col[b + j + 2], v3 = p.col[b + j + 3];
-                if (claim(p, k, v0, u)) after_win(p, sm, ss, nxt, ns, t, v0);
-                if (claim(p, k, v1, u)) after_win(p, sm, ss, nxt, ns, t, v1);
-                if (claim(p, k, v2, u)) after_win(p, sm, ss, nxt, ns, t, v2);
-                if (claim(p, k, v3, u)) after_win(p, sm, ss, nxt, ns, t, v3);
-            }
-            for (; j < deg; ++j) {
-                const int32_t v = p.col[b + j];
-                if (claim(p, k, v, u)) after_win(p, sm, ss, nxt, ns, t, v);
+            for (RowT j = 0; j < deg; j += 4) {
+                int32_t vv[4], uu[4];
+                bool won[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    vv[i] = j + i < deg ? p.col[b + j + i] : -1;
+                    uu[i] = u;
+                }
+                claim_batch(p, k, vv, uu, pre, won);
+                after_win_batch(p, sm, ss, nxt, ns, t, vv, won);
             }
         }
         // warp per vertex
@@ -457,7 +543,7 @@ __device__ void push_binned(const Params<RowT>& p, int k, int qn, RowT qm, const
             const RowT wd = __shfl_sync(kFull, deg, src);
             for (RowT j = lane; j < wd; j += 32) {
                 const int32_t v = p.col[wb + j];
-                if (claim(p, k, v, wu)) after_win(p, sm, ss, nxt, ns, t, v);
+                if (claim(p, k, v, wu, pre)) after_win(p, sm, ss, nxt, ns, t, v);
             }
         }
         // CTA per vertex
@@ -476,7 +562,7 @@ __device__ void push_binned(const Params<RowT>& p, int k, int qn, RowT qm, const
                 const RowT j = j0 + threadIdx.x;
                 if (j < cd) {
                     const int32_t v = p.col[cb + j];
-                    if (claim(p, k, v, cu)) after_win(p, sm, ss, nxt, ns, t, v);
+                    if (claim(p, k, v, cu, pre)) after_win(p, sm, ss, nxt, ns, t, v);
                 }
                 if (__syncthreads_or(ss.stage_n > sm.cap / 2))
                     stage_flush(p, sm, ss, nxt, ns);
@@ -496,7 +582,8 @@ __device__ void push_binned(const Params<RowT>& p, int k, int qn, RowT qm, const
 // each thread binary-searches the window for the owner of its edges.
 template <typename RowT>
 __device__ void push_merge_path(const Params<RowT>& p, int k, int qn, RowT qm,
-                                const Smem<RowT>& sm, SmemScalars& ss, LevelSlot* nxt, Tally& t)
+                                const Smem<RowT>& sm, SmemScalars& ss, LevelSlot* nxt, Tally& t,
+                                bool pre)
 {
     const int cs = k & 1, ns = cs ^ 1;
     const int32_t* qv = p.qv[cs];
@@ -562,13 +649,8 @@ __device__ void push_merge_path(const Params<RowT>& p, int k, int qn, RowT qm,
             }
         }
         bool won[kItems];
-#pragma unroll
-        for (int it = 0; it < kItems; ++it)
-            won[it] = vv[it] >= 0 && claim(p, k, vv[it], uu[it]);
-#pragma unroll
-        for (int it = 0; it < kItems; ++it)
-            if (won[it])
-                after_win(p, sm, ss, nxt, ns, t, vv[it]);
+        claim_batch(p, k, vv, uu, pre, won);
+        after_win_batch(p, sm, ss, nxt, ns, t, vv, won);
         if (threadIdx.x == 0 && r1 < e_hi) {
             int a = 0, c = win;  // last window index with woff <= r1
             while (c - a > 1) {
@@ -586,60 +668,172 @@ __device__ void push_merge_path(const Params<RowT>& p, int k, int qn, RowT qm,
 
 // ------------------------------------------------------------ S7 pull level
 
-// One warp per 32-vertex word of the visited bitmap; lane i owns vertex
-// 32w + i. An unvisited vertex scans its neighbours in CSR order and stops at
-// the first one whose bit is set in the frontier bitmap fb[k & 1]. The warp
-// is the only writer of its visited word and of the next-frontier word, so no
-// atomics are needed; every next-frontier word is written, so the bitmap
-// needs no clearing.
+constexpr int kPullVerts = 4;    // list entries per lane in flight
+constexpr int kChunkBatch = 4;   // chunks whose visited words a warp loads together
+constexpr int kPullRounds = 6;   // two-entry probe rounds before the warp takes a row
+
+// Pull level over the frontier bitmap fb[k & 1] (bit u set iff u is in F_k).
+// A warp owns a chunk of up to 32 visited-bitmap words (up to 1,024 vertices;
+// fewer on small graphs, so that every warp gets chunks): it first compacts
+// the chunk's unvisited vertices into a per-warp list in shared memory, then
+// each lane takes kPullVerts list entries at once (independent chains of
+// row_ptr -> col -> frontier-bitmap loads, so their latencies overlap) and
+// scans each row in CSR order, two entries per round. Most rows resolve in
+// the first round (on R-MAT the median scan is one entry); a row still
+// unresolved after kPullRounds rounds is scanned by the whole warp, 32
+// entries per step, and the lowest hitting lane gives the first frontier
+// neighbour in CSR order, as the per-lane scan does. The warp is the only
+// writer of its chunk's visited and next-frontier words, so no global atomics
+// are needed, and every next-frontier word is written, so that bitmap needs
+// no clearing.
 template <typename RowT>
-__device__ void pull_level(const Params<RowT>& p, int k, Tally& t)
+__device__ __forceinline__ void pull_resolve(const Params<RowT>& p, int k, Tally& t,
+                                             uint32_t* wfound, int w0, int32_t x, int32_t par)
+{
+    p.dist[x] = k + 1;
+    if (p.parent != nullptr)
+        p.parent[x] = par;
+    atomicOr(&wfound[(x >> 5) - w0], 1u << (x & 31));
+    const RowT deg = p.row_ptr[x + 1] - p.row_ptr[x];
+    t.found += 1;
+    t.edges += (unsigned long long)deg;
+    t.maxdeg = (unsigned long long)deg > t.maxdeg ? (unsigned long long)deg : t.maxdeg;
+}
+
+template <typename RowT>
+__device__ void pull_level(const Params<RowT>& p, int k, Tally& t, int32_t* wlist,
+                           uint32_t* wfound)
 {
     const uint32_t* fcur = p.fb[k & 1];
     uint32_t* fnext = p.fb[(k + 1) & 1];
     const int lane = threadIdx.x & 31;
     const int gwarp = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
     const int nwarps = (int)((gridDim.x * blockDim.x) >> 5);
-    for (int w = gwarp; w < p.words; w += nwarps) {
-        const uint32_t vis = ldcg(p.visited + w);
-        uint32_t found = 0;
-        if (vis != kFull) {
-            const int32_t v = (w << 5) + lane;
-            int32_t par = -1;
-            RowT deg = 0;
-            if (!((vis >> lane) & 1u)) {
-                const RowT b = p.row_ptr[v];
-                const RowT e = p.row_ptr[v + 1];
-                deg = e - b;
-                RowT j = b;
-                for (; j + 2 <= e && par < 0; j += 2) {
-                    const int32_t u0 = p.col[j], u1 = p.col[j + 1];
-                    const uint32_t w0 = ldcg(fcur + (u0 >> 5)), w1 = ldcg(fcur + (u1 >> 5));
-                    if ((w0 >> (u0 & 31)) & 1u)
-                        par = u0;
-                    else if ((w1 >> (u1 & 31)) & 1u)
-                        par = u1;
-                }
-                if (par < 0 && j < e) {
-                    const int32_t u0 = p.col[j];
-                    if ((ldcg(fcur + (u0 >> 5)) >> (u0 & 31)) & 1u)
-                        par = u0;
-                }
+    int cw = (p.words + 4 * nwarps - 1) / (4 * nwarps);  // words per chunk
+    cw = cw < 1 ? 1 : (cw > 32 ? 32 : cw);
+    const int nchunks = (p.words + cw - 1) / cw;
+    // Chunks c = gwarp + i * nwarps; the visited words of kChunkBatch of them
+    // are loaded together.
+    for (int cb = gwarp; cb < nchunks; cb += kChunkBatch * nwarps) {
+      uint32_t visb[kChunkBatch];
+#pragma unroll
+      for (int i = 0; i < kChunkBatch; ++i) {
+          const int ci = cb + i * nwarps;
+          const int wi = ci * cw + lane;
+          visb[i] = (ci < nchunks && lane < cw && wi < p.words) ? ldcg(p.visited + wi) : kFull;
+      }
+#pragma unroll 1
+      for (int i = 0; i < kChunkBatch && cb + i * nwarps < nchunks; ++i) {
+        const int c = cb + i * nwarps;
+        const int w0 = c * cw;
+        const int w = w0 + lane;
+        const uint32_t vis = visb[i];
+        const uint32_t todo = ~vis;
+        const int cnt = __popc(todo);
+        const int incl = warp_inclusive_scan(cnt);
+        const int total = __shfl_sync(kFull, incl, 31);
+        wfound[lane] = 0u;
+        if (total > 0) {
+            int pos = incl - cnt;
+            uint32_t m = todo;
+            while (m) {
+                const int b = __ffs(m) - 1;
+                m &= m - 1;
+                wlist[pos++] = (w << 5) + b;
             }
-            found = __ballot_sync(kFull, par >= 0);
-            if (par >= 0) {
-                p.dist[v] = k + 1;
-                if (p.parent != nullptr)
-                    p.parent[v] = par;
-                t.found += 1;
-                t.edges += (unsigned long long)deg;
-                t.maxdeg = (unsigned long long)deg > t.maxdeg ? (unsigned long long)deg : t.maxdeg;
-            }
-            if (lane == 0 && found != 0u)
-                __stcg(p.visited + w, vis | found);
         }
-        if (lane == 0)
-            __stcg(fnext + w, found);
+        __syncwarp();
+        for (int base = 0; base < total; base += 32 * kPullVerts) {
+            int32_t v[kPullVerts], par[kPullVerts];
+            RowT cur[kPullVerts], end[kPullVerts];
+#pragma unroll
+            for (int b = 0; b < kPullVerts; ++b) {
+                const int j = base + b * 32 + lane;
+                v[b] = j < total ? wlist[j] : -1;
+                par[b] = -1;
+                cur[b] = 0;
+                end[b] = 0;
+                if (v[b] >= 0) {
+                    cur[b] = p.row_ptr[v[b]];
+                    end[b] = p.row_ptr[v[b] + 1];
+                }
+            }
+            for (int round = 0; round < kPullRounds; ++round) {
+                int32_t u0[kPullVerts], u1[kPullVerts];
+                uint32_t f0[kPullVerts], f1[kPullVerts];
+#pragma unroll
+                for (int b = 0; b < kPullVerts; ++b) {
+                    u0[b] = -1;
+                    u1[b] = -1;
+                    if (par[b] < 0 && cur[b] < end[b]) {
+                        u0[b] = p.col[cur[b]];
+                        if (cur[b] + 1 < end[b])
+                            u1[b] = p.col[cur[b] + 1];
+                    }
+                }
+#pragma unroll
+                for (int b = 0; b < kPullVerts; ++b) {
+                    f0[b] = u0[b] >= 0 ? ldcg(fcur + (u0[b] >> 5)) : 0u;
+                    f1[b] = u1[b] >= 0 ? ldcg(fcur + (u1[b] >> 5)) : 0u;
+                }
+                bool more = false;
+#pragma unroll
+                for (int b = 0; b < kPullVerts; ++b) {
+                    if (u0[b] >= 0) {
+                        if ((f0[b] >> (u0[b] & 31)) & 1u)
+                            par[b] = u0[b];
+                        else if (u1[b] >= 0 && ((f1[b] >> (u1[b] & 31)) & 1u))
+                            par[b] = u1[b];
+                        else
+                            cur[b] += 2;
+                    }
+                    more |= par[b] < 0 && cur[b] < end[b];
+                }
+                if (!__any_sync(kFull, more))
+                    break;
+            }
+            // Rows still open: the whole warp scans 32 entries per step.
+#pragma unroll
+            for (int b = 0; b < kPullVerts; ++b) {
+                unsigned mm = __ballot_sync(kFull, par[b] < 0 && cur[b] < end[b]);
+                while (mm) {
+                    const int src = __ffs(mm) - 1;
+                    mm &= mm - 1;
+                    const RowT cp = __shfl_sync(kFull, cur[b], src);
+                    const RowT ce = __shfl_sync(kFull, end[b], src);
+                    int32_t hitv = -1;
+                    for (RowT q = cp; q < ce && hitv < 0; q += 32) {
+                        const RowT e = q + lane;
+                        int32_t u = -1;
+                        bool hit = false;
+                        if (e < ce) {
+                            u = p.col[e];
+                            hit = (ldcg(fcur + (u >> 5)) >> (u & 31)) & 1u;
+                        }
+                        const unsigned hm = __ballot_sync(kFull, hit);
+                        if (hm)
+                            hitv = __shfl_sync(kFull, u, __ffs(hm) - 1);
+                    }
+                    if (lane == src) {
+                        par[b] = hitv;
+                        cur[b] = ce;
+                    }
+                }
+            }
+#pragma unroll
+            for (int b = 0; b < kPullVerts; ++b)
+                if (par[b] >= 0)
+                    pull_resolve(p, k, t, wfound, w0, v[b], par[b]);
+        }
+        __syncwarp();
+        if (lane < cw && w < p.words) {
+            const uint32_t f = wfound[lane];
+            if (f != 0u)
+                __stcg(p.visited + w, vis | f);
+            __stcg(fnext + w, f);
+        }
+        __syncwarp();
+      }
     }
 }
 
@@ -674,28 +868,230 @@ template <typename RowT>
 __device__ void bitmap_to_queue(const Params<RowT>& p, int k, const Smem<RowT>& sm,
                                 SmemScalars& ss, LevelSlot* cur)
 {
+    constexpr int kBatch = 4;  // bitmap words per thread loaded together
     const uint32_t* f = p.fb[k & 1];
     const int sel = k & 1;
     const int bd = blockDim.x;
     const int stride = gridDim.x * bd;
-    for (int base = blockIdx.x * bd; base < p.words; base += stride) {
-        const int w = base + threadIdx.x;
-        if (w < p.words) {
-            uint32_t bits = ldcg(f + w);
-            while (bits) {
-                const int bit = __ffs(bits) - 1;
-                bits &= bits - 1;
+    for (int base = blockIdx.x * bd; base < p.words; base += stride * kBatch) {
+        uint32_t bits[kBatch];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            const int w = base + i * stride + threadIdx.x;
+            bits[i] = w < p.words ? ldcg(f + w) : 0u;
+        }
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            const int w = base + i * stride + threadIdx.x;
+            uint32_t b = bits[i];
+            while (b) {
+                const int bit = __ffs(b) - 1;
+                b &= b - 1;
                 const int32_t v = (w << 5) + bit;
-                const RowT b = p.row_ptr[v];
-                const RowT deg = p.row_ptr[v + 1] - b;
+                const RowT rb = p.row_ptr[v];
+                const RowT deg = p.row_ptr[v + 1] - rb;
                 if (deg > 0)
-                    stage_push(p, sm, ss, cur, sel, v, b, deg);
+                    stage_push(p, sm, ss, cur, sel, v, rb, deg);
             }
         }
         if (__syncthreads_or(ss.stage_n > sm.cap / 2))
             stage_flush(p, sm, ss, cur, sel);
     }
     stage_flush(p, sm, ss, cur, sel);
+}
+
+// ------------------------------------------------------------ S9 narrow levels
+
+constexpr int kSoloMaxLevels = 4096;  // levels per single-CTA session
+
+// Narrow push levels on CTA 0 alone (the other CTAs wait at the level's grid
+// barrier). The frontier lives in shared memory (vertex, row start, degree
+// prefix); each level is an edge-balanced pass of at most TILE edges with
+// block barriers only, so the per-level cost is the chain of dependent loads
+// (col, visited atomic, row offsets of the winners) instead of a grid-wide
+// barrier. The session ends at the first level that is empty, too wide, due
+// for a pull, at the depth bound, or after kSoloMaxLevels levels; that level
+// k' is published to the slots and queues exactly as a grid level would have
+// produced it, and its number is left in ctl->solo_resume.
+template <typename RowT>
+__device__ void solo_levels(const Params<RowT>& p, int k, int qn, RowT qm, long long F, long long U,
+                            unsigned long long maxdeg, const Smem<RowT>& sm, SmemScalars& ss,
+                            unsigned long long bar_base)
+{
+    const int bd = blockDim.x;
+    const int tid = threadIdx.x;
+    int32_t* cv = sm.wu;
+    RowT* cb = sm.wbeg;
+    RowT* co = sm.woff;
+    {
+        const int cs = k & 1;
+        for (int i = tid; i < qn; i += bd) {
+            cv[i] = ldcg(p.qv[cs] + i);
+            cb[i] = ldcg(p.qbeg[cs] + i);
+            co[i] = ldcg(p.qoff[cs] + i);
+        }
+        if (tid == 0) {
+            co[qn] = qm;
+            ss.stage_n = 0;
+            ss.solo_found = 0ull;
+            ss.solo_edges = 0ull;
+            ss.solo_maxdeg = 0ull;
+        }
+    }
+    __syncthreads();
+    int j = k;
+    long long Fj = F;
+    long long Uj = U;               // unvisited at level j's start
+    unsigned long long mdj = maxdeg;
+    for (;;) {
+        const unsigned long long t0 = tid == 0 ? global_timer_ns() : 0ull;
+        const RowT M = co[qn];
+        // expand: at most kItems edges per thread, loads batched
+        int32_t vv[kItems], uu[kItems];
+#pragma unroll
+        for (int it = 0; it < kItems; ++it) {
+            const RowT e = (RowT)(it * bd + tid);
+            vv[it] = -1;
+            uu[it] = 0;
+            if (e < M) {
+                int lo = 0, hi = qn;
+                while (hi - lo > 1) {
+                    const int mid = (lo + hi) >> 1;
+                    if (co[mid] <= e)
+                        lo = mid;
+                    else
+                        hi = mid;
+                }
+                uu[it] = cv[lo];
+                vv[it] = p.col[cb[lo] + (e - co[lo])];
+            }
+        }
+        bool won[kItems];
+        claim_batch(p, j, vv, uu, false, won);
+        RowT wb[kItems], we[kItems];
+#pragma unroll
+        for (int it = 0; it < kItems; ++it) {
+            wb[it] = 0;
+            we[it] = 0;
+            if (won[it]) {
+                wb[it] = p.row_ptr[vv[it]];
+                we[it] = p.row_ptr[vv[it] + 1];
+            }
+        }
+#pragma unroll
+        for (int it = 0; it < kItems; ++it) {
+            if (won[it]) {
+                const RowT deg = we[it] - wb[it];
+                atomicAdd(&ss.solo_found, 1ull);
+                atomicAdd(&ss.solo_edges, (unsigned long long)deg);
+                atomicMax(&ss.solo_maxdeg, (unsigned long long)deg);
+                if (deg > 0) {
+                    const int pos = atomicAdd(&ss.stage_n, 1);
+                    sm.sv[pos] = vv[it];
+                    sm.sb[pos] = wb[it];
+                    sm.sd[pos] = deg;
+                }
+            }
+        }
+        __syncthreads();
+        const long long Fn = (long long)ss.solo_found;
+        const unsigned long long en = ss.solo_edges;
+        const unsigned long long mdn = ss.solo_maxdeg;
+        const int nq = ss.stage_n;
+        if (tid == 0 && j < p.stats_cap) {
+            bfs_csr_level_stat st;
+            st.level = j;
+            st.direction = BFS_CSR_DIR_PUSH;
+            st.advance = BFS_CSR_ADV_SINGLE_CTA;
+            st.reserved = 0;
+            st.frontier = Fj;
+            st.frontier_edges = (long long)M;
+            st.unvisited = Uj;
+            st.max_degree = (long long)mdj;
+            st.t_start_ns = (long long)t0;
+            p.stats[j] = st;
+        }
+        const long long Un = Uj - Fn;   // unvisited at level j + 1's start
+        bool stop = Fn == 0 || (p.max_depth >= 0 && j + 1 >= p.max_depth) ||
+                    (long long)en > (long long)p.narrow_max || nq > sm.cap ||
+                    j + 1 - k >= kSoloMaxLevels;
+        if (!stop && p.symmetric && p.direction != BFS_CSR_DIR_PUSH &&
+            (p.direction == BFS_CSR_DIR_PULL || (double)en > p.pull_ratio * (double)Un))
+            stop = true;
+        if (stop) {
+            // Publish F_{j+1}: its queue (staged), its counters, and the
+            // state the grid level j + 1 expects to find. The slots written
+            // here may be the ones the other CTAs read at level k's start, so
+            // first wait (bounded) until every other CTA has arrived at level
+            // k's barrier, which each does right after those reads.
+            const int jn = j + 1;
+            if (tid == 0) {
+                const unsigned long long want = bar_base + gridDim.x - 1;
+                const unsigned long long t0w = global_timer_ns();
+                unsigned int spins = 0;
+                while (ld_acquire_u64(&p.ctl->bar) < want) {
+                    if ((++spins & 63u) == 0u &&
+                        (global_timer_ns() - t0w > (unsigned long long)p.timeout_ns ||
+                         spins > (1u << 30))) {
+                        atomicCAS(&p.ctl->status, BFS_CSR_OK, BFS_CSR_ETIMEOUT);
+                        break;
+                    }
+                }
+            }
+            __syncthreads();
+            if (tid == 0) {
+                LevelSlot* sn = &p.ctl->slot[jn & 3];
+                LevelSlot* sp = &p.ctl->slot[j & 3];
+                LevelSlot* sa = &p.ctl->slot[(jn + 1) & 3];
+                sn->qpack = 0ull;
+                sn->found = (unsigned long long)Fn;
+                sn->fedges = en;
+                sn->maxdeg = mdn;
+                sp->unvisited = Uj;
+                sp->dir = BFS_CSR_DIR_PUSH;
+                sp->adv = BFS_CSR_ADV_SINGLE_CTA;
+                sa->qpack = 0ull;
+                sa->found = 0ull;
+                sa->fedges = 0ull;
+                sa->maxdeg = 0ull;
+                sa->work_next = 0u;
+                sn->work_next = 0u;
+                p.ctl->solo_resume = jn;
+            }
+            stage_flush(p, sm, ss, &p.ctl->slot[jn & 3], jn & 1);
+            return;
+        }
+        // F_{j+1} becomes the current frontier (degree prefix by block scan).
+        {
+            const int per = (nq + bd - 1) / bd;
+            const int lo = min(tid * per, nq), hi = min(lo + per, nq);
+            long long sum = 0;
+            for (int i = lo; i < hi; ++i)
+                sum += (long long)sm.sd[i];
+            long long total;
+            const long long excl = block_exclusive_scan(sum, &total, ss.tmp_ll);
+            RowT run = (RowT)excl;
+            for (int i = lo; i < hi; ++i) {
+                cv[i] = sm.sv[i];
+                cb[i] = sm.sb[i];
+                co[i] = run;
+                run += sm.sd[i];
+            }
+            if (tid == 0) {
+                co[nq] = (RowT)total;
+                ss.stage_n = 0;
+                ss.solo_found = 0ull;
+                ss.solo_edges = 0ull;
+                ss.solo_maxdeg = 0ull;
+            }
+        }
+        __syncthreads();
+        qn = nq;
+        Fj = Fn;
+        Uj = Un;
+        mdj = mdn;
+        ++j;
+    }
 }
 
 // ------------------------------------------------------------ kernels
@@ -724,8 +1120,10 @@ template <typename RowT>
 __host__ __device__ inline size_t level_smem_bytes(int bd)
 {
     const size_t tile = (size_t)bd * kItems;
-    return sizeof(RowT) * (2 * tile + 2 * (tile + 1) + 2 * (size_t)bd) +
-           sizeof(int32_t) * (tile + (tile + 1) + (size_t)bd) + 16;
+    const size_t push = sizeof(RowT) * (2 * tile + 2 * (tile + 1) + 2 * (size_t)bd) +
+                        sizeof(int32_t) * (tile + (tile + 1) + (size_t)bd) + 16;
+    const size_t pull = (size_t)(bd / 32) * (1024 + 32) * sizeof(uint32_t);
+    return push > pull ? push : pull;
 }
 
 // The persistent level loop (S2-S9).
@@ -742,14 +1140,25 @@ __global__ void __launch_bounds__(512, 2) level_kernel(Params<RowT> p)
     unsigned long long target = 0;
     int k = ldcg(&p.ctl->level);
     int budget = p.level_budget;
+    const long long nonisolated = ldcg(&p.ctl->nonisolated);
     const bool leader = blockIdx.x == 0 && threadIdx.x == 0;
     __syncthreads();
 
-    while (ldcg(&p.ctl->done) == 0) {
+    for (;;) {
         LevelSlot* cur = &p.ctl->slot[k & 3];
         LevelSlot* nxt = &p.ctl->slot[(k + 1) & 3];
         const LevelSlot* prv = &p.ctl->slot[(k + 3) & 3];
-        const long long F = (long long)ldcg_u64(&cur->found);
+        // Everything the level start needs, as one batch of independent loads.
+        const unsigned long long found = ldcg_u64(&cur->found);
+        const unsigned long long fedges = ldcg_u64(&cur->fedges);
+        const unsigned long long maxdeg = ldcg_u64(&cur->maxdeg);
+        const long long uprev = ldcg(&prv->unvisited);
+        const int prev_dir = ldcg(&prv->dir);
+        const int done = ldcg(&p.ctl->done);
+        const int status = ldcg(&p.ctl->status);
+        if (done != 0 || status != BFS_CSR_OK)
+            break;
+        const long long F = (long long)found;
         if (F == 0 || (p.max_depth >= 0 && k >= p.max_depth)) {
             if (leader) {
                 const int nl = F == 0 ? k : k + 1;
@@ -765,10 +1174,8 @@ __global__ void __launch_bounds__(512, 2) level_kernel(Params<RowT> p)
         if (budget <= 0)
             break;
         const unsigned long long t_level = leader ? global_timer_ns() : 0ull;
-        const long long mF = (long long)ldcg_u64(&cur->fedges);
-        const unsigned long long maxdeg = ldcg_u64(&cur->maxdeg);
-        const long long U = ldcg(&prv->unvisited) - F;
-        const int prev_dir = ldcg(&prv->dir);
+        const long long mF = (long long)fedges;
+        const long long U = uprev - F;
         int dir;
         if (!p.symmetric || p.direction == BFS_CSR_DIR_PUSH)
             dir = BFS_CSR_DIR_PUSH;
@@ -779,10 +1186,27 @@ __global__ void __launch_bounds__(512, 2) level_kernel(Params<RowT> p)
         Tally t = {0ull, 0ull, 0ull};
         int adv = 0;
 
+        // Narrow push level: CTA 0 runs it (and the following narrow ones)
+        // alone; everyone meets at the barrier and resumes where it stopped.
+        if (dir == BFS_CSR_DIR_PUSH && prev_dir != BFS_CSR_DIR_PULL && p.narrow_max > 0 &&
+            p.level_budget == INT_MAX) {
+            const unsigned long long qp0 = ldcg_u64(&cur->qpack);
+            const int qn0 = (int)(qp0 >> p.eb);
+            const long long qm0 = (long long)(qp0 & ((1ull << p.eb) - 1ull));
+            if (qm0 <= (long long)p.narrow_max && qn0 <= sm.cap) {
+                if (blockIdx.x == 0)
+                    solo_levels(p, k, qn0, (RowT)qm0, F, U, maxdeg, sm, ss, target);
+                if (!grid_barrier(p, target)) break;
+                k = ldcg(&p.ctl->solo_resume);
+                continue;
+            }
+        }
+
         if (dir == BFS_CSR_DIR_PULL) {
             if (leader) {
                 LevelSlot* z = &p.ctl->slot[(k + 2) & 3];
                 z->qpack = 0ull; z->found = 0ull; z->fedges = 0ull; z->maxdeg = 0ull;
+                z->work_next = 0u;
                 cur->unvisited = U;
                 cur->dir = dir;
                 cur->adv = 0;
@@ -794,7 +1218,13 @@ __global__ void __launch_bounds__(512, 2) level_kernel(Params<RowT> p)
                 queue_to_bitmap_set(p, k, qn);
                 if (!grid_barrier(p, target)) break;
             }
-            pull_level(p, k, t);
+            {
+                const int wid = threadIdx.x >> 5;
+                int32_t* wlist = reinterpret_cast<int32_t*>(smem_raw) + wid * 1024;
+                uint32_t* wfound = reinterpret_cast<uint32_t*>(smem_raw) +
+                                   (blockDim.x >> 5) * 1024 + wid * 32;
+                pull_level(p, k, t, wlist, wfound);
+            }
         } else {
             if (prev_dir == BFS_CSR_DIR_PULL) {
                 bitmap_to_queue(p, k, sm, ss, cur);
@@ -813,14 +1243,19 @@ __global__ void __launch_bounds__(512, 2) level_kernel(Params<RowT> p)
             if (leader) {
                 LevelSlot* z = &p.ctl->slot[(k + 2) & 3];
                 z->qpack = 0ull; z->found = 0ull; z->fedges = 0ull; z->maxdeg = 0ull;
+                z->work_next = 0u;
                 cur->unvisited = U;
                 cur->dir = dir;
                 cur->adv = adv;
             }
+            // The plain pre-load of a target's visited word saves an atomic
+            // when most targets are already visited (late, wide levels) and
+            // costs a round trip otherwise.
+            const bool pre = (long long)qm >= 65536 && 2 * U < nonisolated;
             if (adv == BFS_CSR_ADV_MERGE_PATH)
-                push_merge_path(p, k, qn, qm, sm, ss, nxt, t);
+                push_merge_path(p, k, qn, qm, sm, ss, nxt, t, pre);
             else
-                push_binned(p, k, qn, qm, sm, ss, nxt, t);
+                push_binned(p, k, qn, qm, sm, ss, nxt, t, pre);
         }
         if (leader && k < p.stats_cap) {
             bfs_csr_level_stat st;
@@ -923,6 +1358,7 @@ __global__ void init_kernel(Params<RowT> p, const uint32_t* __restrict__ dead, i
             c->slot[s].unvisited = 0;
             c->slot[s].dir = BFS_CSR_DIR_PUSH;
             c->slot[s].adv = 0;
+            c->slot[s].work_next = 0u;
         }
         c->slot[0].found = 1ull;
         c->slot[0].fedges = (unsigned long long)deg;

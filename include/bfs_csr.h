@@ -50,6 +50,7 @@ extern "C" {
                                    or the largest frontier degree >= binned_max_degree */
 #define BFS_CSR_ADV_BINNED 1    /* thread / warp / CTA per vertex by degree */
 #define BFS_CSR_ADV_MERGE_PATH 2 /* edge-balanced: degree prefix + search */
+#define BFS_CSR_ADV_SINGLE_CTA 3 /* (level records only) a narrow level run by one CTA */
 
 /* How a top-down level decides who discovered a vertex. */
 #define BFS_CSR_DISC_BITMAP 0   /* atomicOr on a visited bitmap */
@@ -77,7 +78,11 @@ typedef struct bfs_csr_options {
     int32_t test_unreachable_barrier;/* diagnostics only: nonzero makes the first
                                         device-wide barrier wait for one CTA more than
                                         exists, so the run ends with BFS_CSR_ETIMEOUT */
-    int32_t reserved[7];             /* zero */
+    int32_t narrow_max_edges;        /* push levels whose frontier has at most this many
+                                        edges (and vertices) run on one CTA without
+                                        grid barriers; 0 disables; capped at the CTA's
+                                        stage (block_threads * 4); default 2048 */
+    int32_t reserved[6];             /* zero */
 } bfs_csr_options;
 
 /* Per-level record, kept when the run completes (see bfs_csr_level_stats). */

@@ -106,6 +106,28 @@ def test_random_small_graphs_every_source(fbc):
         check_against_oracle(fbc, g, range(n))
 
 
+def test_many_back_to_back_small_searches(fbc):
+    """Tiny searches finish in a few microseconds, so CTAs that start late
+    overlap with CTA 0's single-CTA levels. Many in a row, every direction,
+    must all end correctly (a slot race between them once surfaced as a
+    barrier timeout)."""
+    graphs = [graphgen.from_csr(np.array([0, 2, 4, 7, 8], np.int32),
+                                np.array([1, 2, 0, 2, 0, 1, 3, 2], np.int32), True),
+              graphgen.path_graph(9), graphgen.star_graph(17), graphgen.clique_graph(5)]
+    for g in graphs:
+        for direction in (0, 1, 2):
+            bfs = fbc.BfsCsr(_dev(g.row_ptr), _dev(g.col), True,
+                             fbc.default_options(direction=direction,
+                                                 barrier_timeout_ns=2_000_000_000))
+            want = [oracle.bfs(g.row_ptr, g.col, s, want_parent=False) for s in range(g.n)]
+            for rep in range(25):
+                for s in range(g.n):
+                    dist, _, levels = bfs.search(s, want_parent=False)
+                    assert np.array_equal(dist.cpu().numpy(), want[s][0]), (g.name, s, rep)
+                    assert levels == want[s][2]
+            bfs.close()
+
+
 def test_corner_cases(fbc):
     cases = [
         (graphgen.from_edges(1, [], []), [0]),
@@ -182,6 +204,8 @@ OPTION_MATRIX = [
     dict(small_max_degree=1, cta_min_degree=2, advance=1),
     dict(small_max_degree=4, cta_min_degree=64, advance=1, direction=1),
     dict(merge_path_min_frontier=0), dict(pull_ratio=0.0), dict(pull_ratio=100.0),
+    dict(narrow_max_edges=0), dict(narrow_max_edges=8), dict(narrow_max_edges=2048, advance=2),
+    dict(narrow_max_edges=100000, block_threads=128), dict(narrow_max_edges=64, discovery=1),
 ]
 
 
