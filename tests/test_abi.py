@@ -56,7 +56,8 @@ int main(void) {
   F(bfs_csr_options, binned_max_degree); F(bfs_csr_options, pull_ratio);
   F(bfs_csr_options, max_depth); F(bfs_csr_options, validate); F(bfs_csr_options, block_threads);
   F(bfs_csr_options, grid_blocks); F(bfs_csr_options, barrier_timeout_ns);
-  F(bfs_csr_options, test_unreachable_barrier); F(bfs_csr_options, reserved);
+  F(bfs_csr_options, test_unreachable_barrier); F(bfs_csr_options, narrow_max_edges);
+  F(bfs_csr_options, reserved);
   F(bfs_csr_level_stat, level); F(bfs_csr_level_stat, direction); F(bfs_csr_level_stat, advance);
   F(bfs_csr_level_stat, frontier); F(bfs_csr_level_stat, frontier_edges);
   F(bfs_csr_level_stat, unvisited); F(bfs_csr_level_stat, max_degree);
