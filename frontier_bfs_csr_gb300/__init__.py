@@ -59,15 +59,16 @@ class bfs_csr_options(ctypes.Structure):
         ("cta_min_degree", ctypes.c_int32),
         ("merge_path_min_frontier", ctypes.c_int32),
         ("binned_max_degree", ctypes.c_int32),
-        ("pull_ratio", ctypes.c_double),
+        ("pull_alpha", ctypes.c_double),
         ("max_depth", ctypes.c_int32),
         ("validate", ctypes.c_int32),
         ("block_threads", ctypes.c_int32),
         ("grid_blocks", ctypes.c_int32),
         ("barrier_timeout_ns", ctypes.c_int64),
         ("test_unreachable_barrier", ctypes.c_int32),
+        ("push_beta", ctypes.c_int32),
         ("narrow_max_edges", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 6),
+        ("reserved", ctypes.c_int32 * 5),
     ]
 
 

@@ -120,7 +120,7 @@ int check_options(const bfs_csr_options& o)
     if (o.loop_mode < BFS_CSR_LOOP_PERSISTENT || o.loop_mode > BFS_CSR_LOOP_HOST) return BFS_CSR_EINVAL;
     if (o.small_max_degree < 1 || o.cta_min_degree < o.small_max_degree) return BFS_CSR_EINVAL;
     if (o.merge_path_min_frontier < 0 || o.binned_max_degree < 1) return BFS_CSR_EINVAL;
-    if (!(o.pull_ratio >= 0.0)) return BFS_CSR_EINVAL;
+    if (!(o.pull_alpha >= 0.0) || o.push_beta < 0) return BFS_CSR_EINVAL;
     if (o.block_threads != 0 && (o.block_threads < 64 || o.block_threads > 512 || o.block_threads % 32))
         return BFS_CSR_EINVAL;
     if (o.grid_blocks < 0 || o.barrier_timeout_ns <= 0 || o.narrow_max_edges < 0)
@@ -175,6 +175,9 @@ Params<RowT> make_params(bfs_csr_t* h, int32_t* d_dist, int32_t* d_parent, int32
     p.dist = d_dist;
     p.parent = d_parent;
     p.visited = reinterpret_cast<uint32_t*>(w + h->L.visited);
+    p.dead = reinterpret_cast<const uint32_t*>(w + h->L.dead);
+    p.vec_out = ((reinterpret_cast<uintptr_t>(d_dist) & 15u) == 0 &&
+                 (reinterpret_cast<uintptr_t>(d_parent) & 15u) == 0) ? 1 : 0;
     p.fb[0] = reinterpret_cast<uint32_t*>(w + h->L.fb0);
     p.fb[1] = reinterpret_cast<uint32_t*>(w + h->L.fb1);
     p.qv[0] = reinterpret_cast<int32_t*>(w + h->L.qv0);
@@ -195,7 +198,9 @@ Params<RowT> make_params(bfs_csr_t* h, int32_t* d_dist, int32_t* d_parent, int32
     p.cta_min = h->opt.cta_min_degree;
     p.mp_min_frontier = h->opt.merge_path_min_frontier;
     p.binned_max_deg = h->opt.binned_max_degree;
-    p.pull_ratio = h->opt.pull_ratio;
+    p.pull_alpha = h->opt.pull_alpha;
+    p.push_beta = h->opt.push_beta;
+    p.nnz = h->nnz;
     p.max_depth = h->opt.max_depth;
     p.symmetric = h->symmetric;
     p.level_budget = INT_MAX;
@@ -356,7 +361,8 @@ int bfs_csr_default_options(bfs_csr_options* o)
     o->cta_min_degree = 256;
     o->merge_path_min_frontier = 4096;
     o->binned_max_degree = 8192;
-    o->pull_ratio = 1.0;
+    o->pull_alpha = 14.0;
+    o->push_beta = 24;
     o->max_depth = -1;
     o->validate = 1;
     o->block_threads = 0;

@@ -60,8 +60,9 @@ struct __align__(16) LevelSlot {
     long long unvisited;        // U_k: non-isolated vertices unreached at level k
     int dir;                    // direction used at level k
     int adv;                    // advance used at level k (push levels)
-    unsigned int work_next;     // next chunk of level k handed out to a warp
+    unsigned int work_next;     // (unused) chunk counter
     unsigned int pad_slot;
+    long long unvisited_edges;  // m_U at level k: out-degree sum of U_k
 };
 
 struct __align__(128) Ctl {
@@ -90,6 +91,8 @@ struct Params {
     int32_t* dist;
     int32_t* parent;            // may be null
     uint32_t* visited;
+    const uint32_t* dead;       // degree-0 vertices and padding bits (symmetric CSR)
+    int vec_out;                // dist and parent are 16-byte aligned
     uint32_t* fb[2];            // frontier bitmaps, F_k in fb[k & 1]
     int32_t* qv[2];             // frontier queues, F_k in qv[k & 1]
     RowT* qbeg[2];              // row start of each queued vertex
@@ -101,7 +104,9 @@ struct Params {
     int eb;                     // edge bits of LevelSlot::qpack
     int direction, advance, discovery;
     int small_max, cta_min, mp_min_frontier, binned_max_deg;
-    double pull_ratio;
+    double pull_alpha;
+    int push_beta;
+    long long nnz;
     int max_depth;
     int symmetric;
     int level_budget;           // levels this launch may run
@@ -242,7 +247,7 @@ struct Smem {
     // compaction stage (S6)
     int32_t* sv;      // vertex
     RowT* sb;         // row start
-    RowT* sd;         // degree
+    int32_t* sd;      // degree (a row holds fewer than 2^31 entries)
     int cap;
     // merge-path window (S4)
     RowT* woff;
@@ -298,7 +303,7 @@ __device__ __forceinline__ void stage_push(const Params<RowT>& p, const Smem<Row
     if (pos < sm.cap) {
         sm.sv[pos] = v;
         sm.sb[pos] = b;
-        sm.sd[pos] = deg;
+        sm.sd[pos] = (int32_t)deg;
     } else {
         append_direct(p, nxt, qsel, v, b, deg);
     }
@@ -662,8 +667,13 @@ __device__ void push_merge_path(const Params<RowT>& p, int k, int qn, RowT qm,
             }
             ss.cur = cur + a;
         }
-        stage_flush(p, sm, ss, nxt, ns);
+        // Flush once the stage is half full (every round when most edges
+        // discover, every few rounds otherwise: fewer global atomics). A round
+        // can add at most TILE entries; any excess is appended directly.
+        if (__syncthreads_or(ss.stage_n > sm.cap / 2))
+            stage_flush(p, sm, ss, nxt, ns);
     }
+    stage_flush(p, sm, ss, nxt, ns);
 }
 
 // ------------------------------------------------------------ S7 pull level
@@ -686,6 +696,7 @@ constexpr int kPullRounds = 6;   // two-entry probe rounds before the warp takes
 // writer of its chunk's visited and next-frontier words, so no global atomics
 // are needed, and every next-frontier word is written, so that bitmap needs
 // no clearing.
+
 template <typename RowT>
 __device__ __forceinline__ void pull_resolve(const Params<RowT>& p, int k, Tally& t,
                                              uint32_t* wfound, int w0, int32_t x, int32_t par)
@@ -900,6 +911,28 @@ __device__ void bitmap_to_queue(const Params<RowT>& p, int k, const Smem<RowT>& 
     stage_flush(p, sm, ss, cur, sel);
 }
 
+// S2: the direction of level k. Only symmetric graphs may pull. In AUTO
+// mode this is the direction-optimising rule with exact device counts: after
+// a push level, pull once the frontier's edges m_F exceed m_U / pull_alpha
+// (m_U = edges of the vertices not reached yet); after a pull level, return
+// to push once |F| falls below N / push_beta (N = vertices of nonzero
+// degree). The pages' rule compares |F| * average degree with |U| (PMPP
+// ch. 15 notes, section 15.7); exact m_F and m_U make the comparison robust to
+// frontiers whose degrees are far from the average (hub-heavy levels).
+template <typename RowT>
+__device__ __forceinline__ int choose_direction(const Params<RowT>& p, int prev_dir, long long F,
+                                                long long mF, long long mU, long long nonisolated)
+{
+    if (!p.symmetric || p.direction == BFS_CSR_DIR_PUSH)
+        return BFS_CSR_DIR_PUSH;
+    if (p.direction == BFS_CSR_DIR_PULL)
+        return BFS_CSR_DIR_PULL;
+    if (prev_dir == BFS_CSR_DIR_PULL && p.push_beta > 0)
+        return (double)F * (double)p.push_beta < (double)nonisolated ? BFS_CSR_DIR_PUSH
+                                                                      : BFS_CSR_DIR_PULL;
+    return (double)mF * p.pull_alpha > (double)mU ? BFS_CSR_DIR_PULL : BFS_CSR_DIR_PUSH;
+}
+
 // ------------------------------------------------------------ S9 narrow levels
 
 constexpr int kSoloMaxLevels = 4096;  // levels per single-CTA session
@@ -915,8 +948,8 @@ constexpr int kSoloMaxLevels = 4096;  // levels per single-CTA session
 // produced it, and its number is left in ctl->solo_resume.
 template <typename RowT>
 __device__ void solo_levels(const Params<RowT>& p, int k, int qn, RowT qm, long long F, long long U,
-                            unsigned long long maxdeg, const Smem<RowT>& sm, SmemScalars& ss,
-                            unsigned long long bar_base)
+                            long long mU, unsigned long long maxdeg, const Smem<RowT>& sm,
+                            SmemScalars& ss, unsigned long long bar_base, long long nonisolated)
 {
     const int bd = blockDim.x;
     const int tid = threadIdx.x;
@@ -942,6 +975,7 @@ __device__ void solo_levels(const Params<RowT>& p, int k, int qn, RowT qm, long 
     int j = k;
     long long Fj = F;
     long long Uj = U;               // unvisited at level j's start
+    long long mUj = mU;             // their edges
     unsigned long long mdj = maxdeg;
     for (;;) {
         const unsigned long long t0 = tid == 0 ? global_timer_ns() : 0ull;
@@ -989,7 +1023,7 @@ __device__ void solo_levels(const Params<RowT>& p, int k, int qn, RowT qm, long 
                     const int pos = atomicAdd(&ss.stage_n, 1);
                     sm.sv[pos] = vv[it];
                     sm.sb[pos] = wb[it];
-                    sm.sd[pos] = deg;
+                    sm.sd[pos] = (int32_t)deg;
                 }
             }
         }
@@ -1012,11 +1046,12 @@ __device__ void solo_levels(const Params<RowT>& p, int k, int qn, RowT qm, long 
             p.stats[j] = st;
         }
         const long long Un = Uj - Fn;   // unvisited at level j + 1's start
+        const long long mUn = mUj - (long long)en;
         bool stop = Fn == 0 || (p.max_depth >= 0 && j + 1 >= p.max_depth) ||
                     (long long)en > (long long)p.narrow_max || nq > sm.cap ||
                     j + 1 - k >= kSoloMaxLevels;
-        if (!stop && p.symmetric && p.direction != BFS_CSR_DIR_PUSH &&
-            (p.direction == BFS_CSR_DIR_PULL || (double)en > p.pull_ratio * (double)Un))
+        if (!stop && choose_direction(p, BFS_CSR_DIR_PUSH, Fn, (long long)en, mUn, nonisolated) !=
+                         BFS_CSR_DIR_PUSH)
             stop = true;
         if (stop) {
             // Publish F_{j+1}: its queue (staged), its counters, and the
@@ -1048,6 +1083,7 @@ __device__ void solo_levels(const Params<RowT>& p, int k, int qn, RowT qm, long 
                 sn->fedges = en;
                 sn->maxdeg = mdn;
                 sp->unvisited = Uj;
+                sp->unvisited_edges = mUj;
                 sp->dir = BFS_CSR_DIR_PUSH;
                 sp->adv = BFS_CSR_ADV_SINGLE_CTA;
                 sa->qpack = 0ull;
@@ -1089,6 +1125,7 @@ __device__ void solo_levels(const Params<RowT>& p, int k, int qn, RowT qm, long 
         qn = nq;
         Fj = Fn;
         Uj = Un;
+        mUj = mUn;
         mdj = mdn;
         ++j;
     }
@@ -1096,6 +1133,10 @@ __device__ void solo_levels(const Params<RowT>& p, int k, int qn, RowT qm, long 
 
 // ------------------------------------------------------------ kernels
 
+// Dynamic shared memory: the compaction stage (row starts, degrees, vertices)
+// and, after it, one region used either as the merge-path / single-CTA window
+// (offsets, row starts, vertices) or as the binned advance's CTA-per-vertex
+// list; pull levels reuse the whole buffer for their per-warp lists.
 template <typename RowT>
 __device__ __forceinline__ Smem<RowT> carve_smem(unsigned char* raw, int bd)
 {
@@ -1105,14 +1146,15 @@ __device__ __forceinline__ Smem<RowT> carve_smem(unsigned char* raw, int bd)
     sm.cap = tile;
     sm.wcap = tile + 1;
     sm.sb = reinterpret_cast<RowT*>(q); q += sizeof(RowT) * sm.cap;
-    sm.sd = reinterpret_cast<RowT*>(q); q += sizeof(RowT) * sm.cap;
+    sm.sd = reinterpret_cast<int32_t*>(q); q += sizeof(int32_t) * sm.cap;
+    sm.sv = reinterpret_cast<int32_t*>(q); q += sizeof(int32_t) * sm.cap;
+    unsigned char* x = q;
     sm.woff = reinterpret_cast<RowT*>(q); q += sizeof(RowT) * sm.wcap;
     sm.wbeg = reinterpret_cast<RowT*>(q); q += sizeof(RowT) * sm.wcap;
-    sm.lb = reinterpret_cast<RowT*>(q); q += sizeof(RowT) * bd;
-    sm.ld = reinterpret_cast<RowT*>(q); q += sizeof(RowT) * bd;
-    sm.sv = reinterpret_cast<int32_t*>(q); q += sizeof(int32_t) * sm.cap;
-    sm.wu = reinterpret_cast<int32_t*>(q); q += sizeof(int32_t) * sm.wcap;
-    sm.lu = reinterpret_cast<int32_t*>(q);
+    sm.wu = reinterpret_cast<int32_t*>(q);
+    sm.lb = reinterpret_cast<RowT*>(x);
+    sm.ld = sm.lb + bd;
+    sm.lu = reinterpret_cast<int32_t*>(sm.ld + bd);
     return sm;
 }
 
@@ -1120,8 +1162,7 @@ template <typename RowT>
 __host__ __device__ inline size_t level_smem_bytes(int bd)
 {
     const size_t tile = (size_t)bd * kItems;
-    const size_t push = sizeof(RowT) * (2 * tile + 2 * (tile + 1) + 2 * (size_t)bd) +
-                        sizeof(int32_t) * (tile + (tile + 1) + (size_t)bd) + 16;
+    const size_t push = (sizeof(RowT) + 8) * tile + (2 * sizeof(RowT) + 4) * (tile + 1) + 16;
     const size_t pull = (size_t)(bd / 32) * (1024 + 32) * sizeof(uint32_t);
     return push > pull ? push : pull;
 }
@@ -1153,6 +1194,7 @@ __global__ void __launch_bounds__(512, 2) level_kernel(Params<RowT> p)
         const unsigned long long fedges = ldcg_u64(&cur->fedges);
         const unsigned long long maxdeg = ldcg_u64(&cur->maxdeg);
         const long long uprev = ldcg(&prv->unvisited);
+        const long long ueprev = ldcg(&prv->unvisited_edges);
         const int prev_dir = ldcg(&prv->dir);
         const int done = ldcg(&p.ctl->done);
         const int status = ldcg(&p.ctl->status);
@@ -1176,13 +1218,8 @@ __global__ void __launch_bounds__(512, 2) level_kernel(Params<RowT> p)
         const unsigned long long t_level = leader ? global_timer_ns() : 0ull;
         const long long mF = (long long)fedges;
         const long long U = uprev - F;
-        int dir;
-        if (!p.symmetric || p.direction == BFS_CSR_DIR_PUSH)
-            dir = BFS_CSR_DIR_PUSH;
-        else if (p.direction == BFS_CSR_DIR_PULL)
-            dir = BFS_CSR_DIR_PULL;
-        else
-            dir = (double)mF > p.pull_ratio * (double)U ? BFS_CSR_DIR_PULL : BFS_CSR_DIR_PUSH;
+        const long long mU = ueprev - mF;
+        const int dir = choose_direction(p, prev_dir, F, mF, mU, nonisolated);
         Tally t = {0ull, 0ull, 0ull};
         int adv = 0;
 
@@ -1195,7 +1232,8 @@ __global__ void __launch_bounds__(512, 2) level_kernel(Params<RowT> p)
             const long long qm0 = (long long)(qp0 & ((1ull << p.eb) - 1ull));
             if (qm0 <= (long long)p.narrow_max && qn0 <= sm.cap) {
                 if (blockIdx.x == 0)
-                    solo_levels(p, k, qn0, (RowT)qm0, F, U, maxdeg, sm, ss, target);
+                    solo_levels(p, k, qn0, (RowT)qm0, F, U, mU, maxdeg, sm, ss, target,
+                                nonisolated);
                 if (!grid_barrier(p, target)) break;
                 k = ldcg(&p.ctl->solo_resume);
                 continue;
@@ -1208,6 +1246,7 @@ __global__ void __launch_bounds__(512, 2) level_kernel(Params<RowT> p)
                 z->qpack = 0ull; z->found = 0ull; z->fedges = 0ull; z->maxdeg = 0ull;
                 z->work_next = 0u;
                 cur->unvisited = U;
+                cur->unvisited_edges = mU;
                 cur->dir = dir;
                 cur->adv = 0;
             }
@@ -1245,6 +1284,7 @@ __global__ void __launch_bounds__(512, 2) level_kernel(Params<RowT> p)
                 z->qpack = 0ull; z->found = 0ull; z->fedges = 0ull; z->maxdeg = 0ull;
                 z->work_next = 0u;
                 cur->unvisited = U;
+                cur->unvisited_edges = mU;
                 cur->dir = dir;
                 cur->adv = adv;
             }
@@ -1356,6 +1396,7 @@ __global__ void init_kernel(Params<RowT> p, const uint32_t* __restrict__ dead, i
             c->slot[s].fedges = 0ull;
             c->slot[s].maxdeg = 0ull;
             c->slot[s].unvisited = 0;
+            c->slot[s].unvisited_edges = 0;
             c->slot[s].dir = BFS_CSR_DIR_PUSH;
             c->slot[s].adv = 0;
             c->slot[s].work_next = 0u;
@@ -1372,12 +1413,13 @@ __global__ void init_kernel(Params<RowT> p, const uint32_t* __restrict__ dead, i
         // U_0 = nonisolated vertices other than the source: slot 3 holds U_{-1}
         // such that U_0 = U_{-1} - |F_0|.
         c->slot[3].unvisited = c->nonisolated - (deg > 0 ? 1 : 0) + 1;
+        c->slot[3].unvisited_edges = p.nnz;
         c->slot[3].dir = BFS_CSR_DIR_PUSH;
     }
 }
 
-// S0: CSR checks (row_ptr[0] = 0, row_ptr[n] = nnz, non-decreasing, col in
-// range). Flags: bit 0 row_ptr, bit 1 col.
+// S0: CSR checks (row_ptr[0] = 0, row_ptr[n] = nnz, non-decreasing with rows
+// shorter than 2^31 entries, col in range). Flags: bit 0 row_ptr, bit 1 col.
 template <typename RowT>
 __global__ void validate_kernel(const RowT* __restrict__ row_ptr, const int32_t* __restrict__ col,
                                 int64_t n, int64_t nnz, int* flags)
@@ -1387,9 +1429,11 @@ __global__ void validate_kernel(const RowT* __restrict__ row_ptr, const int32_t*
     int bad = 0;
     if (tid == 0 && (row_ptr[0] != 0 || (int64_t)row_ptr[n] != nnz))
         bad |= 1;
-    for (int64_t i = tid; i < n; i += stride)
-        if (row_ptr[i + 1] < row_ptr[i])
-            bad |= 1;
+    for (int64_t i = tid; i < n; i += stride) {
+        const int64_t d = (int64_t)row_ptr[i + 1] - (int64_t)row_ptr[i];
+        if (d < 0 || d > (int64_t)INT32_MAX)
+            bad |= 1;  // decreasing, or a row too long for 32-bit degrees
+    }
     for (int64_t e = tid; e < nnz; e += stride) {
         const int32_t v = col[e];
         if (v < 0 || (int64_t)v >= n)

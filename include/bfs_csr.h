@@ -41,7 +41,7 @@ extern "C" {
  * neighbour in the frontier bitmap; it needs in-edges, so it is only
  * available for a symmetric CSR (PMPP ch. 15 notes, section 15.3 push/pull
  * and section 15.7 direction-optimised BFS). */
-#define BFS_CSR_DIR_AUTO 0      /* pull when frontier edges > pull_ratio * unvisited */
+#define BFS_CSR_DIR_AUTO 0      /* direction-optimising rule, see pull_alpha / push_beta */
 #define BFS_CSR_DIR_PUSH 1
 #define BFS_CSR_DIR_PULL 2      /* every level is bottom-up */
 
@@ -69,7 +69,9 @@ typedef struct bfs_csr_options {
     int32_t cta_min_degree;          /* binned: degree >= this -> CTA per vertex (256) */
     int32_t merge_path_min_frontier; /* auto advance threshold on |F| (4096) */
     int32_t binned_max_degree;       /* auto advance threshold on max degree (8192) */
-    double pull_ratio;               /* auto direction: pull iff m_F > pull_ratio*|U| (1.0) */
+    double pull_alpha;               /* auto direction after a push level: pull iff
+                                        m_F * pull_alpha > m_U, the edges of the vertices
+                                        not reached yet (14) */
     int32_t max_depth;               /* label only vertices within this many hops; <0: all */
     int32_t validate;                /* nonzero: check the CSR at create (O(nnz)) */
     int32_t block_threads;           /* CTA size of the level kernel; 0 = default (512) */
@@ -78,11 +80,14 @@ typedef struct bfs_csr_options {
     int32_t test_unreachable_barrier;/* diagnostics only: nonzero makes the first
                                         device-wide barrier wait for one CTA more than
                                         exists, so the run ends with BFS_CSR_ETIMEOUT */
+    int32_t push_beta;               /* auto direction after a pull level: push again iff
+                                        |F| * push_beta < vertices of nonzero degree (24);
+                                        0: apply the pull_alpha rule instead */
     int32_t narrow_max_edges;        /* push levels whose frontier has at most this many
                                         edges (and vertices) run on one CTA without
                                         grid barriers; 0 disables; capped at the CTA's
                                         stage (block_threads * 4); default 2048 */
-    int32_t reserved[6];             /* zero */
+    int32_t reserved[5];             /* zero */
 } bfs_csr_options;
 
 /* Per-level record, kept when the run completes (see bfs_csr_level_stats). */

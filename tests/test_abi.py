@@ -53,10 +53,11 @@ int main(void) {
   F(bfs_csr_options, direction); F(bfs_csr_options, advance); F(bfs_csr_options, discovery);
   F(bfs_csr_options, loop_mode); F(bfs_csr_options, small_max_degree);
   F(bfs_csr_options, cta_min_degree); F(bfs_csr_options, merge_path_min_frontier);
-  F(bfs_csr_options, binned_max_degree); F(bfs_csr_options, pull_ratio);
+  F(bfs_csr_options, binned_max_degree); F(bfs_csr_options, pull_alpha);
   F(bfs_csr_options, max_depth); F(bfs_csr_options, validate); F(bfs_csr_options, block_threads);
   F(bfs_csr_options, grid_blocks); F(bfs_csr_options, barrier_timeout_ns);
-  F(bfs_csr_options, test_unreachable_barrier); F(bfs_csr_options, narrow_max_edges);
+  F(bfs_csr_options, test_unreachable_barrier); F(bfs_csr_options, push_beta);
+  F(bfs_csr_options, narrow_max_edges);
   F(bfs_csr_options, reserved);
   F(bfs_csr_level_stat, level); F(bfs_csr_level_stat, direction); F(bfs_csr_level_stat, advance);
   F(bfs_csr_level_stat, frontier); F(bfs_csr_level_stat, frontier_edges);
@@ -92,7 +93,8 @@ def test_defaults(fbc):
     assert o.discovery == fbc.BFS_CSR_DISC_BITMAP and o.loop_mode == fbc.BFS_CSR_LOOP_PERSISTENT
     assert (o.small_max_degree, o.cta_min_degree) == (32, 256)
     assert o.merge_path_min_frontier == 4096  # Gunrock paper's static hybrid threshold
-    assert o.pull_ratio == 1.0 and o.max_depth == -1 and o.validate == 1
+    assert o.pull_alpha == 14.0 and o.push_beta == 24
+    assert o.max_depth == -1 and o.validate == 1
     assert o.barrier_timeout_ns > 0 and o.test_unreachable_barrier == 0
 
 

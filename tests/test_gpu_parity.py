@@ -203,7 +203,8 @@ OPTION_MATRIX = [
     dict(grid_blocks=3, advance=1), dict(grid_blocks=7, advance=2, direction=1),
     dict(small_max_degree=1, cta_min_degree=2, advance=1),
     dict(small_max_degree=4, cta_min_degree=64, advance=1, direction=1),
-    dict(merge_path_min_frontier=0), dict(pull_ratio=0.0), dict(pull_ratio=100.0),
+    dict(merge_path_min_frontier=0), dict(pull_alpha=0.0), dict(pull_alpha=1e9),
+    dict(push_beta=0), dict(push_beta=1000000, pull_alpha=1.0),
     dict(narrow_max_edges=0), dict(narrow_max_edges=8), dict(narrow_max_edges=2048, advance=2),
     dict(narrow_max_edges=100000, block_threads=128), dict(narrow_max_edges=64, discovery=1),
 ]
