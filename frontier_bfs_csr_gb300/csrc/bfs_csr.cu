@@ -26,7 +26,7 @@ constexpr int kStatsCap = 1 << 16;
 constexpr int kDefaultBlock = 512;
 
 struct Layout {
-    size_t ctl, visited, dead, fb0, fb1, qv0, qv1, qbeg0, qbeg1, qoff0, qoff1, stats, total;
+    size_t ctl, visited, dead, head, fb0, fb1, qv0, qv1, qbeg0, qbeg1, qoff0, qoff1, stats, total;
 };
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -45,6 +45,7 @@ Layout make_layout(int64_t n, int row_ptr_64)
     L.ctl = take(sizeof(Ctl));
     L.visited = take(words * 4);
     L.dead = take(words * 4);
+    L.head = take((size_t)n * 8);
     L.fb0 = take(words * 4);
     L.fb1 = take(words * 4);
     L.qv0 = take((size_t)n * 4);
@@ -176,6 +177,7 @@ Params<RowT> make_params(bfs_csr_t* h, int32_t* d_dist, int32_t* d_parent, int32
     p.parent = d_parent;
     p.visited = reinterpret_cast<uint32_t*>(w + h->L.visited);
     p.dead = reinterpret_cast<const uint32_t*>(w + h->L.dead);
+    p.head = reinterpret_cast<const int2*>(w + h->L.head);
     p.vec_out = ((reinterpret_cast<uintptr_t>(d_dist) & 15u) == 0 &&
                  (reinterpret_cast<uintptr_t>(d_parent) & 15u) == 0) ? 1 : 0;
     p.fb[0] = reinterpret_cast<uint32_t*>(w + h->L.fb0);
@@ -235,6 +237,9 @@ int prepare(bfs_csr_t* h, cudaStream_t s)
     }
     fbc::dead_kernel<RowT><<<init_grid(h), 256, 0, s>>>(
         rp, (int32_t)h->n, h->words, reinterpret_cast<uint32_t*>(w + h->L.dead), &ctl->nonisolated);
+    FBC_CUDA(h, cudaGetLastError());
+    fbc::head_kernel<RowT><<<init_grid(h), 256, 0, s>>>(rp, h->col, (int32_t)h->n,
+                                                         reinterpret_cast<int2*>(w + h->L.head));
     FBC_CUDA(h, cudaGetLastError());
     FBC_CUDA(h, cudaStreamSynchronize(s));
     return configure_grid<RowT>(h);
@@ -635,6 +640,7 @@ constexpr int64_t kNoAllocMaxN = BFS_CSR_NOALLOC_MAX_VERTICES;
 // to 256 bytes.
 constexpr size_t kNoAllocBytes =
     (sizeof(Ctl) + 256) + 4 * ((size_t)kNoAllocMaxN / 8 + 256) +
+    ((size_t)kNoAllocMaxN * 8 + 256) +
     2 * ((size_t)kNoAllocMaxN * 4 + 256) + 4 * ((size_t)kNoAllocMaxN * 4 + 256) +
     ((size_t)kStatsCap * sizeof(bfs_csr_level_stat) + 256);
 

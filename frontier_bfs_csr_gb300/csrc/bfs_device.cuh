@@ -92,6 +92,7 @@ struct Params {
     int32_t* parent;            // may be null
     uint32_t* visited;
     const uint32_t* dead;       // degree-0 vertices and padding bits (symmetric CSR)
+    const int2* head;           // per vertex: (first neighbour or -1, degree)
     int vec_out;                // dist and parent are 16-byte aligned
     uint32_t* fb[2];            // frontier bitmaps, F_k in fb[k & 1]
     int32_t* qv[2];             // frontier queues, F_k in qv[k & 1]
@@ -678,7 +679,7 @@ __device__ void push_merge_path(const Params<RowT>& p, int k, int qn, RowT qm,
 
 // ------------------------------------------------------------ S7 pull level
 
-constexpr int kPullVerts = 4;    // list entries per lane in flight
+constexpr int kPullVerts = 2;    // list entries per lane in flight
 constexpr int kChunkBatch = 4;   // chunks whose visited words a warp loads together
 constexpr int kPullRounds = 6;   // two-entry probe rounds before the warp takes a row
 
@@ -688,8 +689,10 @@ constexpr int kPullRounds = 6;   // two-entry probe rounds before the warp takes
 // the chunk's unvisited vertices into a per-warp list in shared memory, then
 // each lane takes kPullVerts list entries at once (independent chains of
 // row_ptr -> col -> frontier-bitmap loads, so their latencies overlap) and
-// scans each row in CSR order, two entries per round. Most rows resolve in
-// the first round (on R-MAT the median scan is one entry); a row still
+// scans each row in CSR order: the first entry comes from the head array
+// (first neighbour and degree, read nearly sequentially), the rest two entries
+// per round from col. Most rows resolve on the first entry (on R-MAT the
+// median scan is one entry), so most of them never touch row_ptr or col; a row still
 // unresolved after kPullRounds rounds is scanned by the whole warp, 32
 // entries per step, and the lowest hitting lane gives the first frontier
 // neighbour in CSR order, as the per-lane scan does. The warp is the only
@@ -699,13 +702,13 @@ constexpr int kPullRounds = 6;   // two-entry probe rounds before the warp takes
 
 template <typename RowT>
 __device__ __forceinline__ void pull_resolve(const Params<RowT>& p, int k, Tally& t,
-                                             uint32_t* wfound, int w0, int32_t x, int32_t par)
+                                             uint32_t* wfound, int w0, int32_t x, int32_t par,
+                                             int32_t deg)
 {
     p.dist[x] = k + 1;
     if (p.parent != nullptr)
         p.parent[x] = par;
     atomicOr(&wfound[(x >> 5) - w0], 1u << (x & 31));
-    const RowT deg = p.row_ptr[x + 1] - p.row_ptr[x];
     t.found += 1;
     t.edges += (unsigned long long)deg;
     t.maxdeg = (unsigned long long)deg > t.maxdeg ? (unsigned long long)deg : t.maxdeg;
@@ -755,21 +758,44 @@ __device__ void pull_level(const Params<RowT>& p, int k, Tally& t, int32_t* wlis
         }
         __syncwarp();
         for (int base = 0; base < total; base += 32 * kPullVerts) {
-            int32_t v[kPullVerts], par[kPullVerts];
+            int32_t v[kPullVerts], par[kPullVerts], deg[kPullVerts];
             RowT cur[kPullVerts], end[kPullVerts];
+            // Round 0: the first neighbour from the head array (no row_ptr or
+            // col access); only rows that miss it load their offsets.
+            {
+                int2 hd[kPullVerts];
 #pragma unroll
-            for (int b = 0; b < kPullVerts; ++b) {
-                const int j = base + b * 32 + lane;
-                v[b] = j < total ? wlist[j] : -1;
-                par[b] = -1;
-                cur[b] = 0;
-                end[b] = 0;
-                if (v[b] >= 0) {
-                    cur[b] = p.row_ptr[v[b]];
-                    end[b] = p.row_ptr[v[b] + 1];
+                for (int b = 0; b < kPullVerts; ++b) {
+                    const int j = base + b * 32 + lane;
+                    v[b] = j < total ? wlist[j] : -1;
+                    hd[b] = v[b] >= 0 ? __ldg(p.head + v[b]) : make_int2(-1, 0);
+                }
+                uint32_t f0[kPullVerts];
+#pragma unroll
+                for (int b = 0; b < kPullVerts; ++b)
+                    f0[b] = hd[b].x >= 0 ? ldcg(fcur + (hd[b].x >> 5)) : 0u;
+#pragma unroll
+                for (int b = 0; b < kPullVerts; ++b) {
+                    deg[b] = hd[b].y;
+                    par[b] = (hd[b].x >= 0 && ((f0[b] >> (hd[b].x & 31)) & 1u)) ? hd[b].x : -1;
+                    cur[b] = 0;
+                    end[b] = 0;
+                }
+#pragma unroll
+                for (int b = 0; b < kPullVerts; ++b) {
+                    if (v[b] >= 0 && par[b] < 0 && deg[b] > 1) {
+                        cur[b] = p.row_ptr[v[b]] + 1;
+                        end[b] = cur[b] + (RowT)(deg[b] - 1);
+                    }
                 }
             }
             for (int round = 0; round < kPullRounds; ++round) {
+                bool any = false;
+#pragma unroll
+                for (int b = 0; b < kPullVerts; ++b)
+                    any |= par[b] < 0 && cur[b] < end[b];
+                if (!__any_sync(kFull, any))
+                    break;
                 int32_t u0[kPullVerts], u1[kPullVerts];
                 uint32_t f0[kPullVerts], f1[kPullVerts];
 #pragma unroll
@@ -834,7 +860,7 @@ __device__ void pull_level(const Params<RowT>& p, int k, Tally& t, int32_t* wlis
 #pragma unroll
             for (int b = 0; b < kPullVerts; ++b)
                 if (par[b] >= 0)
-                    pull_resolve(p, k, t, wfound, w0, v[b], par[b]);
+                    pull_resolve(p, k, t, wfound, w0, v[b], par[b], deg[b]);
         }
         __syncwarp();
         if (lane < cw && w < p.words) {
@@ -1464,6 +1490,22 @@ __global__ void dead_kernel(const RowT* __restrict__ row_ptr, int32_t n, int32_t
     }
     if (lane == 0 && live)
         atomicAdd(reinterpret_cast<unsigned long long*>(nonisolated), (unsigned long long)live);
+}
+
+// Per-vertex head of the row: (col[row_ptr[v]] or -1, degree), 8 bytes, so
+// that a pull level reads one nearly sequential array to test a vertex's first
+// neighbour instead of a row_ptr entry and a random col block. Derived from
+// the CSR at create time; the rows themselves are never copied.
+template <typename RowT>
+__global__ void head_kernel(const RowT* __restrict__ row_ptr, const int32_t* __restrict__ col,
+                            int32_t n, int2* head)
+{
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < n; v += stride) {
+        const RowT b = row_ptr[v];
+        const RowT d = row_ptr[v + 1] - b;
+        head[v] = make_int2(d > 0 ? col[b] : -1, (int32_t)d);
+    }
 }
 
 }  // namespace fbc
