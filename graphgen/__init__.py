@@ -301,7 +301,8 @@ def _generate(cfg: int) -> Graph:
 
 
 def _cache_dir() -> str:
-    return os.environ.get("BFS_GRAPH_CACHE", os.path.join("/tmp", "frontier_bfs_graphs"))
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    return os.environ.get("BFS_GRAPH_CACHE", os.path.join(root, ".graph_cache"))
 
 
 def _source_digest() -> str:

@@ -66,13 +66,14 @@ int main(void) {
   return 0;
 }
 '''
-    d = tempfile.mkdtemp()
-    c = os.path.join(d, "layout.c")
-    exe = os.path.join(d, "layout")
-    with open(c, "w") as f:
-        f.write(src)
-    subprocess.check_call(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), c, "-o", exe])
-    out = subprocess.run([exe], capture_output=True, text=True, check=True).stdout
+    os.makedirs(os.path.join(ROOT, "_build"), exist_ok=True)
+    with tempfile.TemporaryDirectory(dir=os.path.join(ROOT, "_build")) as d:
+        c = os.path.join(d, "layout.c")
+        exe = os.path.join(d, "layout")
+        with open(c, "w") as f:
+            f.write(src)
+        subprocess.check_call(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), c, "-o", exe])
+        out = subprocess.run([exe], capture_output=True, text=True, check=True).stdout
     return {k: int(v) for k, v in (line.split() for line in out.strip().splitlines())}
 
 

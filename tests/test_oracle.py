@@ -326,7 +326,9 @@ MUTANTS = [
 def test_pins_reject_oracle_mutants(old, new, golden, monkeypatch):
     src = open(os.path.join(os.path.dirname(oracle.__file__), "bfs_oracle.c")).read()
     assert old in src, "mutation site vanished"
-    tmp = tempfile.mkdtemp()
+    build_dir = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "_build")
+    os.makedirs(build_dir, exist_ok=True)
+    tmp = tempfile.mkdtemp(dir=build_dir)
     try:
         pkg = os.path.join(tmp, "oracle")
         shutil.copytree(os.path.dirname(oracle.__file__), pkg,
