@@ -565,23 +565,11 @@ int bfs_csr_run_host(bfs_csr_handle h, int64_t source, const void* h_row_ptr, co
         if (h->nnz > 0)
             FBC_CUDA(h, cudaMemcpyAsync(h->d_col_own, h_col, (size_t)h->nnz * 4,
                                         cudaMemcpyHostToDevice, s));
-        if (h->opt.validate) {
-            Ctl* ctl = reinterpret_cast<Ctl*>(h->ws + h->L.ctl);
-            FBC_CUDA(h, cudaMemsetAsync(&ctl->validate_flags, 0, sizeof(int), s));
-            int flags = 0;
-            if (h->row_ptr_64)
-                fbc::validate_kernel<int64_t><<<init_grid(h), 256, 0, s>>>(
-                    static_cast<const int64_t*>(h->row_ptr), h->col, h->n, h->nnz, &ctl->validate_flags);
-            else
-                fbc::validate_kernel<int32_t><<<init_grid(h), 256, 0, s>>>(
-                    static_cast<const int32_t*>(h->row_ptr), h->col, h->n, h->nnz, &ctl->validate_flags);
-            FBC_CUDA(h, cudaGetLastError());
-            FBC_CUDA(h, cudaMemcpyAsync(&flags, &ctl->validate_flags, sizeof(int),
-                                        cudaMemcpyDeviceToHost, s));
-            FBC_CUDA(h, cudaStreamSynchronize(s));
-            if (flags != 0)
-                return BFS_CSR_EINVAL;
-        }
+        // A new CSR: validate it and re-derive the dead bitmap, the
+        // non-isolated count and the head array, as create does.
+        const int prc = h->row_ptr_64 ? prepare<int64_t>(h, s) : prepare<int32_t>(h, s);
+        if (prc != BFS_CSR_OK)
+            return prc;
     }
     int rc = bfs_csr_run(h, source, h->d_dist_own, h_parent ? h->d_parent_own : nullptr,
                          h->d_levels_own, stream);

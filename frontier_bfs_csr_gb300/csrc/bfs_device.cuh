@@ -688,14 +688,15 @@ constexpr int kPullRounds = 6;   // two-entry probe rounds before the warp takes
 // fewer on small graphs, so that every warp gets chunks): it first compacts
 // the chunk's unvisited vertices into a per-warp list in shared memory, then
 // each lane takes kPullVerts list entries at once (independent chains of
-// row_ptr -> col -> frontier-bitmap loads, so their latencies overlap) and
-// scans each row in CSR order: the first entry comes from the head array
-// (first neighbour and degree, read nearly sequentially), the rest two entries
-// per round from col. Most rows resolve on the first entry (on R-MAT the
-// median scan is one entry), so most of them never touch row_ptr or col; a row still
-// unresolved after kPullRounds rounds is scanned by the whole warp, 32
-// entries per step, and the lowest hitting lane gives the first frontier
-// neighbour in CSR order, as the per-lane scan does. The warp is the only
+// head -> frontier-bitmap loads, so their latencies overlap). The first test
+// is the probe neighbour stored in the head array (read nearly sequentially,
+// with the degree); most rows found by a wide pull level resolve there and
+// never touch row_ptr or col. A row that misses is scanned in CSR order, two
+// entries per round; one still unresolved after kPullRounds rounds is scanned
+// by the whole warp, 32 entries per step, and the lowest hitting lane gives
+// the first frontier neighbour in CSR order, as the per-lane scan does. The
+// parent is thus the probe neighbour when it is in F_k, else the first
+// neighbour in F_k in CSR order. The warp is the only
 // writer of its chunk's visited and next-frontier words, so no global atomics
 // are needed, and every next-frontier word is written, so that bitmap needs
 // no clearing.
@@ -760,8 +761,9 @@ __device__ void pull_level(const Params<RowT>& p, int k, Tally& t, int32_t* wlis
         for (int base = 0; base < total; base += 32 * kPullVerts) {
             int32_t v[kPullVerts], par[kPullVerts], deg[kPullVerts];
             RowT cur[kPullVerts], end[kPullVerts];
-            // Round 0: the first neighbour from the head array (no row_ptr or
-            // col access); only rows that miss it load their offsets.
+            // Round 0: the probe neighbour from the head array (no row_ptr or
+            // col access); only rows that miss it load their offsets and scan
+            // the whole row (a one-entry row has nothing more to scan).
             {
                 int2 hd[kPullVerts];
 #pragma unroll
@@ -784,8 +786,8 @@ __device__ void pull_level(const Params<RowT>& p, int k, Tally& t, int32_t* wlis
 #pragma unroll
                 for (int b = 0; b < kPullVerts; ++b) {
                     if (v[b] >= 0 && par[b] < 0 && deg[b] > 1) {
-                        cur[b] = p.row_ptr[v[b]] + 1;
-                        end[b] = cur[b] + (RowT)(deg[b] - 1);
+                        cur[b] = p.row_ptr[v[b]];
+                        end[b] = cur[b] + (RowT)deg[b];
                     }
                 }
             }
@@ -1492,10 +1494,18 @@ __global__ void dead_kernel(const RowT* __restrict__ row_ptr, int32_t n, int32_t
         atomicAdd(reinterpret_cast<unsigned long long*>(nonisolated), (unsigned long long)live);
 }
 
-// Per-vertex head of the row: (col[row_ptr[v]] or -1, degree), 8 bytes, so
-// that a pull level reads one nearly sequential array to test a vertex's first
-// neighbour instead of a row_ptr entry and a random col block. Derived from
-// the CSR at create time; the rows themselves are never copied.
+// Per-vertex head of the row: (a probe neighbour or -1, degree), 8 bytes, so
+// that a pull level tests one likely parent of each unvisited vertex from a
+// nearly sequential array instead of a row_ptr entry and a random col block.
+// The probe neighbour is the one of highest degree among the first
+// kHeadScan entries of the row (the earliest on ties). High-degree vertices
+// are reached first in a search from almost any source, so for a vertex
+// found by a pull level that neighbour is usually in the current frontier;
+// on R-MAT inputs the first neighbour in CSR order, the plain choice, is
+// there for only about a third of them. Derived from the CSR at create time;
+// the rows themselves are never copied.
+constexpr int kHeadScan = 64;
+
 template <typename RowT>
 __global__ void head_kernel(const RowT* __restrict__ row_ptr, const int32_t* __restrict__ col,
                             int32_t n, int2* head)
@@ -1504,7 +1514,29 @@ __global__ void head_kernel(const RowT* __restrict__ row_ptr, const int32_t* __r
     for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < n; v += stride) {
         const RowT b = row_ptr[v];
         const RowT d = row_ptr[v + 1] - b;
-        head[v] = make_int2(d > 0 ? col[b] : -1, (int32_t)d);
+        int32_t best = d > 0 ? col[b] : -1;
+        if (d > 1) {
+            const int m = d < (RowT)kHeadScan ? (int)d : kHeadScan;
+            RowT best_deg = -1;
+            for (int i = 0; i < m; i += 8) {
+                int32_t u[8];
+                RowT du[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    u[j] = i + j < m ? col[b + i + j] : -1;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    du[j] = u[j] >= 0 ? row_ptr[u[j] + 1] - row_ptr[u[j]] : (RowT)-1;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    if (du[j] > best_deg) {
+                        best_deg = du[j];
+                        best = u[j];
+                    }
+                }
+            }
+        }
+        head[v] = make_int2(best, (int32_t)d);
     }
 }
 

@@ -122,8 +122,11 @@ int bfs_csr_workspace_bytes(int64_t n, int64_t nnz, int row_ptr_64,
  * be NULL (the library allocates and frees it) or caller memory of at least
  * bfs_csr_workspace_bytes, 256-byte aligned, owned by the caller. With
  * opt->validate the CSR is checked on the device; a malformed CSR gives
- * BFS_CSR_EINVAL. Limits: 1 <= n < 2^31, nnz < 2^31 for int32 row_ptr.
- * The call synchronises `stream`.
+ * BFS_CSR_EINVAL. The call then derives, in the workspace, a bitmap of the
+ * degree-0 vertices and a head array (per vertex: one probe neighbour, the
+ * highest-degree one among the row's first 64 entries, and the degree) in
+ * one pass over the rows. Limits: 1 <= n < 2^31, nnz < 2^31 for int32
+ * row_ptr. The call synchronises `stream`.
  */
 int bfs_csr_create(bfs_csr_handle *out, int64_t n, int64_t nnz,
                    const void *d_row_ptr, int row_ptr_64, const int32_t *d_col,
@@ -172,7 +175,9 @@ int bfs_csr_level_stats(bfs_csr_handle h, bfs_csr_level_stat *host_buf,
  * bfs_csr_create_host allocates device copies of the CSR, the workspace and
  * the outputs, uploads the CSR and validates it as bfs_csr_create does.
  * bfs_csr_run_host then (1) re-uploads the CSR from h_row_ptr/h_col when they
- * are non-NULL (same n and nnz; checked again when validation is on), (2)
+ * are non-NULL (same n and nnz; checked again when validation is on) and
+ * re-derives the per-vertex data create builds from it (the degree-0 bitmap
+ * and the head array: one pass over the rows), (2)
  * runs the search, (3) copies dist, parent (if h_parent != NULL) and the level
  * count back, and synchronises `stream` before returning the run's status.
  * Pinned host memory makes the copies asynchronous and fast.

@@ -335,3 +335,25 @@ def test_host_memory_api(fbc):
         levels = h.run(int(s), dist)  # resident CSR, no parent
         assert np.array_equal(dist, want) and levels == want_levels
     h.close()
+
+
+def test_host_memory_api_new_csr_of_the_same_size(fbc):
+    """Each upload of a different CSR with the same n and nnz is searched as
+    that graph: the degree-0 bitmap and the head array are re-derived."""
+    n = 5000
+    v = np.arange(n - 1, dtype=np.uint32)
+    cyc = np.arange(n - 1, dtype=np.uint32)
+    graphs = [graphgen.star_graph(n), graphgen.path_graph(n),
+              graphgen.from_edges(n, cyc, (cyc + 1) % (n - 1)),  # vertex n-1 isolated
+              graphgen.from_edges(n, np.full(n - 1, n - 1, np.uint32), v)]  # star at n-1
+    assert len({g.nnz for g in graphs}) == 1
+    h = fbc.BfsCsrHost(graphs[0].row_ptr, graphs[0].col, True)
+    for g in graphs:
+        for s in (0, 1, n // 2):
+            dist = np.empty(n, np.int32)
+            parent = np.empty(n, np.int32)
+            levels = h.run(s, dist, parent, row_ptr=g.row_ptr, col=g.col)
+            want, _, want_levels = oracle.bfs(g.row_ptr, g.col, s, want_parent=False)
+            assert np.array_equal(dist, want) and levels == want_levels, g.name
+            assert oracle.check_parent(g.row_ptr, g.col, s, dist, parent)[0] == 0
+    h.close()
