@@ -295,18 +295,35 @@ __device__ void append_direct(const Params<RowT>& p, LevelSlot* nxt, int qsel,
     p.qoff[qsel][slot] = (RowT)eoff;
 }
 
+// Stage v (row start b, degree deg) when take is set. Every converged lane
+// of the warp calls it; one shared atomic per warp reserves the slots of all
+// its taking lanes (a per-lane atomic on the one counter serialises when
+// most edges discover). A slot past the stage's capacity goes straight to
+// the queue.
 template <typename RowT>
 __device__ __forceinline__ void stage_push(const Params<RowT>& p, const Smem<RowT>& sm,
                                            SmemScalars& ss, LevelSlot* nxt, int qsel,
-                                           int32_t v, RowT b, RowT deg)
+                                           int32_t v, RowT b, RowT deg, bool take)
 {
-    const int pos = atomicAdd(&ss.stage_n, 1);
-    if (pos < sm.cap) {
-        sm.sv[pos] = v;
-        sm.sb[pos] = b;
-        sm.sd[pos] = (int32_t)deg;
-    } else {
-        append_direct(p, nxt, qsel, v, b, deg);
+    const unsigned act = __activemask();
+    const unsigned m = __ballot_sync(act, take);
+    if (m == 0u)
+        return;
+    const int lane = threadIdx.x & 31;
+    const int leader = __ffs(m) - 1;
+    int base = 0;
+    if (lane == leader)
+        base = atomicAdd(&ss.stage_n, __popc(m));
+    base = __shfl_sync(act, base, leader);
+    if (take) {
+        const int pos = base + __popc(m & ((1u << lane) - 1u));
+        if (pos < sm.cap) {
+            sm.sv[pos] = v;
+            sm.sb[pos] = b;
+            sm.sd[pos] = (int32_t)deg;
+        } else {
+            append_direct(p, nxt, qsel, v, b, deg);
+        }
     }
 }
 
@@ -453,19 +470,22 @@ __device__ __forceinline__ void claim_batch(const Params<RowT>& p, int k, const 
     }
 }
 
-// After a win: read v's row, count it, and queue it when it has edges.
+// After a claim: a winner reads v's row, counts it, and is queued when it
+// has edges. Every converged lane calls it (won false for the others).
 template <typename RowT>
 __device__ __forceinline__ void after_win(const Params<RowT>& p, const Smem<RowT>& sm,
                                           SmemScalars& ss, LevelSlot* nxt, int qsel, Tally& t,
-                                          int32_t v)
+                                          int32_t v, bool won)
 {
-    const RowT b = p.row_ptr[v];
-    const RowT deg = p.row_ptr[v + 1] - b;
-    t.found += 1;
-    t.edges += (unsigned long long)deg;
-    t.maxdeg = (unsigned long long)deg > t.maxdeg ? (unsigned long long)deg : t.maxdeg;
-    if (deg > 0)
-        stage_push(p, sm, ss, nxt, qsel, v, b, deg);
+    RowT b = 0, deg = 0;
+    if (won) {
+        b = p.row_ptr[v];
+        deg = p.row_ptr[v + 1] - b;
+        t.found += 1;
+        t.edges += (unsigned long long)deg;
+        t.maxdeg = (unsigned long long)deg > t.maxdeg ? (unsigned long long)deg : t.maxdeg;
+    }
+    stage_push(p, sm, ss, nxt, qsel, v, b, deg, won && deg > 0);
 }
 
 // after_win for a batch: the row offsets of all winners are loaded together.
@@ -487,14 +507,13 @@ __device__ __forceinline__ void after_win_batch(const Params<RowT>& p, const Sme
     }
 #pragma unroll
     for (int i = 0; i < N; ++i) {
-        if (!won[i])
-            continue;
         const RowT deg = e[i] - b[i];
-        t.found += 1;
-        t.edges += (unsigned long long)deg;
-        t.maxdeg = (unsigned long long)deg > t.maxdeg ? (unsigned long long)deg : t.maxdeg;
-        if (deg > 0)
-            stage_push(p, sm, ss, nxt, qsel, v[i], b[i], deg);
+        if (won[i]) {
+            t.found += 1;
+            t.edges += (unsigned long long)deg;
+            t.maxdeg = (unsigned long long)deg > t.maxdeg ? (unsigned long long)deg : t.maxdeg;
+        }
+        stage_push(p, sm, ss, nxt, qsel, v[i], b[i], deg, won[i] && deg > 0);
     }
 }
 
@@ -549,7 +568,7 @@ __device__ void push_binned(const Params<RowT>& p, int k, int qn, RowT qm, const
             const RowT wd = __shfl_sync(kFull, deg, src);
             for (RowT j = lane; j < wd; j += 32) {
                 const int32_t v = p.col[wb + j];
-                if (claim(p, k, v, wu, pre)) after_win(p, sm, ss, nxt, ns, t, v);
+                after_win(p, sm, ss, nxt, ns, t, v, claim(p, k, v, wu, pre));
             }
         }
         // CTA per vertex
@@ -568,7 +587,7 @@ __device__ void push_binned(const Params<RowT>& p, int k, int qn, RowT qm, const
                 const RowT j = j0 + threadIdx.x;
                 if (j < cd) {
                     const int32_t v = p.col[cb + j];
-                    if (claim(p, k, v, cu, pre)) after_win(p, sm, ss, nxt, ns, t, v);
+                    after_win(p, sm, ss, nxt, ns, t, v, claim(p, k, v, cu, pre));
                 }
                 if (__syncthreads_or(ss.stage_n > sm.cap / 2))
                     stage_flush(p, sm, ss, nxt, ns);
@@ -624,25 +643,33 @@ __device__ void push_merge_path(const Params<RowT>& p, int k, int qn, RowT qm,
     }
     __syncthreads();
 
+    // cur: first queue entry the tile touches. The window holds queue entries
+    // [wbase, wbase + wn). Every thread computes both from shared state read
+    // before the end-of-tile barrier, so they are uniform and the window is
+    // only rewritten after every read of it in the previous tile.
+    int cur = ss.cur, wbase = 0, wn = 0;
+    bool covered = false;
     for (RowT r0 = e_lo; r0 < e_hi; r0 += tile) {
         const RowT r1 = r0 + (RowT)tile < e_hi ? r0 + (RowT)tile : e_hi;
-        const int cur = ss.cur;
-        const int win = min(tile + 1, qn - cur);
-        for (int x = threadIdx.x; x < win; x += bd) {
-            sm.woff[x] = ldcg(qo + cur + x);
-            sm.wbeg[x] = ldcg(qb + cur + x);
-            sm.wu[x] = ldcg(qv + cur + x);
+        if (!covered) {
+            wbase = cur;
+            wn = min(tile + 1, qn - cur);
+            for (int x = threadIdx.x; x < wn; x += bd) {
+                sm.woff[x] = ldcg(qo + cur + x);
+                sm.wbeg[x] = ldcg(qb + cur + x);
+                sm.wu[x] = ldcg(qv + cur + x);
+            }
+            __syncthreads();
         }
-        __syncthreads();
         int32_t vv[kItems], uu[kItems];
-        int lo = 0;
+        int lo = cur - wbase;
 #pragma unroll
         for (int it = 0; it < kItems; ++it) {
             const RowT e = r0 + (RowT)(it * bd + threadIdx.x);
             vv[it] = -1;
             uu[it] = 0;
             if (e < r1) {
-                int hi = win;
+                int hi = wn;
                 while (hi - lo > 1) {
                     const int mid = (lo + hi) >> 1;
                     if (sm.woff[mid] <= e)
@@ -657,8 +684,12 @@ __device__ void push_merge_path(const Params<RowT>& p, int k, int qn, RowT qm,
         bool won[kItems];
         claim_batch(p, k, vv, uu, pre, won);
         after_win_batch(p, sm, ss, nxt, ns, t, vv, won);
-        if (threadIdx.x == 0 && r1 < e_hi) {
-            int a = 0, c = win;  // last window index with woff <= r1
+        if (r1 < e_hi) {
+            // The next tile starts at the last entry with offset <= r1; the
+            // window still serves it when it holds every entry up to the last
+            // one starting before the next tile's end (a frontier of few
+            // high-degree vertices keeps one window for many tiles).
+            int a = cur - wbase, c = wn;
             while (c - a > 1) {
                 const int mid = (a + c) >> 1;
                 if (sm.woff[mid] <= r1)
@@ -666,7 +697,9 @@ __device__ void push_merge_path(const Params<RowT>& p, int k, int qn, RowT qm,
                 else
                     c = mid;
             }
-            ss.cur = cur + a;
+            cur = wbase + a;
+            const RowT r2 = r1 + (RowT)tile < e_hi ? r1 + (RowT)tile : e_hi;
+            covered = wbase + wn == qn || sm.woff[wn - 1] >= r2;
         }
         // Flush once the stage is half full (every round when most edges
         // discover, every few rounds otherwise: fewer global atomics). A round
@@ -929,8 +962,7 @@ __device__ void bitmap_to_queue(const Params<RowT>& p, int k, const Smem<RowT>& 
                 const int32_t v = (w << 5) + bit;
                 const RowT rb = p.row_ptr[v];
                 const RowT deg = p.row_ptr[v + 1] - rb;
-                if (deg > 0)
-                    stage_push(p, sm, ss, cur, sel, v, rb, deg);
+                stage_push(p, sm, ss, cur, sel, v, rb, deg, deg > 0);
             }
         }
         if (__syncthreads_or(ss.stage_n > sm.cap / 2))
@@ -1040,20 +1072,26 @@ __device__ void solo_levels(const Params<RowT>& p, int k, int qn, RowT qm, long 
                 we[it] = p.row_ptr[vv[it] + 1];
             }
         }
+        // Tallies per warp, then one shared atomic per warp and counter; the
+        // level has at most one stage of winners, so no slot overflows.
+        unsigned long long f_loc = 0ull, e_loc = 0ull, m_loc = 0ull;
 #pragma unroll
         for (int it = 0; it < kItems; ++it) {
+            const RowT deg = we[it] - wb[it];
             if (won[it]) {
-                const RowT deg = we[it] - wb[it];
-                atomicAdd(&ss.solo_found, 1ull);
-                atomicAdd(&ss.solo_edges, (unsigned long long)deg);
-                atomicMax(&ss.solo_maxdeg, (unsigned long long)deg);
-                if (deg > 0) {
-                    const int pos = atomicAdd(&ss.stage_n, 1);
-                    sm.sv[pos] = vv[it];
-                    sm.sb[pos] = wb[it];
-                    sm.sd[pos] = (int32_t)deg;
-                }
+                f_loc += 1ull;
+                e_loc += (unsigned long long)deg;
+                m_loc = (unsigned long long)deg > m_loc ? (unsigned long long)deg : m_loc;
             }
+            stage_push(p, sm, ss, nullptr, 0, vv[it], wb[it], deg, won[it] && deg > 0);
+        }
+        f_loc = warp_sum(f_loc);
+        e_loc = warp_sum(e_loc);
+        m_loc = warp_max(m_loc);
+        if ((tid & 31) == 0 && f_loc != 0ull) {
+            atomicAdd(&ss.solo_found, f_loc);
+            atomicAdd(&ss.solo_edges, e_loc);
+            atomicMax(&ss.solo_maxdeg, m_loc);
         }
         __syncthreads();
         const long long Fn = (long long)ss.solo_found;
