@@ -14,13 +14,15 @@
 //      CTA per vertex, PMPP ch. 15 notes section 15.7; the three size classes
 //      of the Gunrock paper's section 4.4 as quoted on the Gunrock reading
 //      page, step 4) or edge-balanced (merge-path: an exclusive prefix of the
-//      frontier's degrees plus a search per CTA and per edge; Gunrock reading
-//      page steps 4-5, and "The Frontier Model for Parallel BFS" section 22.3).
+//      frontier's degrees plus a search per warp and per edge; Gunrock
+//      reading page steps 4-5, and "The Frontier Model for Parallel BFS"
+//      section 22.3).
 //   S5 discovery: atomicOr on a visited bitmap, or atomicCAS on dist
 //      (Day 38 claimVertex; ch. 22 sections 22.1-22.2); exactly one winner
 //      per vertex writes dist and parent.
 //   S6 compaction: winners are staged in shared memory and flushed with one
-//      global atomic per CTA batch (the privatised queue of PMPP ch. 15 notes,
+//      global atomic per CTA (or, in the merge path, per warp) batch (the
+//      privatised queue of PMPP ch. 15 notes,
 //      section 15.6, without its silent drop on overflow: a full stage makes
 //      the thread append directly).
 //   S7 pull level over a frontier bitmap, one warp per 32-vertex word: no
@@ -30,9 +32,10 @@
 //      frontier (Gunrock's convergence test, read on the device).
 //
 // The exclusive prefix the merge-path search needs is produced for free by
-// the compaction: a CTA reserves its queue slots and its edge range with one
-// 64-bit atomicAdd on a packed (count, edges) counter, so queue order and
-// edge order agree and qoff[] is a valid exclusive scan of the degrees.
+// the compaction: a CTA or warp reserves its queue slots and its edge range
+// with one 64-bit atomicAdd on a packed (count, edges) counter, so queue
+// order and edge order agree and qoff[] is a valid exclusive scan of the
+// degrees.
 #pragma once
 
 #include <climits>
@@ -43,7 +46,7 @@
 
 namespace fbc {
 
-constexpr int kItems = 4;        // edges per thread per merge-path round
+constexpr int kItems = 4;        // edges per thread per single-CTA level round
 constexpr int kSlots = 4;        // rotating per-level counter slots
 constexpr int kMaxBlock = 1024;
 constexpr unsigned kFull = 0xffffffffu;
@@ -250,7 +253,7 @@ struct Smem {
     RowT* sb;         // row start
     int32_t* sd;      // degree (a row holds fewer than 2^31 entries)
     int cap;
-    // merge-path window (S4)
+    // single-CTA level frontier (offsets, row starts, vertices)
     RowT* woff;
     RowT* wbeg;
     int32_t* wu;
@@ -600,114 +603,217 @@ __device__ void push_binned(const Params<RowT>& p, int k, int qn, RowT qm, const
     }
 }
 
-// Merge-path advance: CTA c owns the edge range [c*M/G, (c+1)*M/G) of the
-// frontier's concatenated adjacency lists. One 32-ary search over qoff finds
-// the first vertex; each round then stages the offsets of at most TILE + 1
-// vertices in shared memory (every queued vertex has at least one edge) and
-// each thread binary-searches the window for the owner of its edges.
+// Warp-level merge path. The level's edge range [0, m_F) is split evenly over
+// all warps of the grid; a warp walks its share in batches of up to kWItems
+// items of 32 consecutive edges, with no CTA-wide barrier, so every warp is
+// an independent chain of loads (a CTA-wide tile loop gives the SM only as
+// many chains as it has CTAs, and every tile waits for the slowest warp).
+// The warp keeps a window of 32 queue entries in registers, one per lane:
+// the entry's edge offset, row start and vertex, and the end of its range.
+// For an item starting at edge e, the entry of e is the first lane whose
+// range ends after e, and lane l's entry is that one plus the number of
+// entries starting in (e, e + l], read from one OR-reduction of start bits.
+// 32 consecutive edges span at most 32 entries (every queued vertex has an
+// edge), so a window whose first entry holds e covers a whole item. Winners
+// go to the warp's own slice of the stage; a flush moves it to the next
+// queue with one packed atomic per warp.
+constexpr int kWarpStage = 256;  // stage entries per warp
+constexpr int kWItems = 4;       // 32-edge items per warp batch
+
 template <typename RowT>
-__device__ void push_merge_path(const Params<RowT>& p, int k, int qn, RowT qm,
-                                const Smem<RowT>& sm, SmemScalars& ss, LevelSlot* nxt, Tally& t,
-                                bool pre)
+struct WarpStage {
+    RowT* b;
+    int32_t* v;
+    int32_t* d;
+};
+
+template <typename RowT>
+__device__ __forceinline__ WarpStage<RowT> warp_stage(unsigned char* raw)
+{
+    unsigned char* q = raw + (size_t)(threadIdx.x >> 5) * kWarpStage * (sizeof(RowT) + 8);
+    WarpStage<RowT> w;
+    w.b = reinterpret_cast<RowT*>(q);
+    w.v = reinterpret_cast<int32_t*>(q + sizeof(RowT) * kWarpStage);
+    w.d = w.v + kWarpStage;
+    return w;
+}
+
+// Move the warp's n staged vertices to the next queue: one packed atomic
+// reserves their slots and edge range; they are written 32 at a time with
+// the exclusive prefix of their degrees.
+template <typename RowT>
+__device__ void warp_flush(const Params<RowT>& p, const WarpStage<RowT>& ws, int n,
+                           LevelSlot* nxt, int qsel)
+{
+    __syncwarp();
+    const int lane = threadIdx.x & 31;
+    unsigned long long sum = 0ull;
+    for (int i = lane; i < n; i += 32)
+        sum += (unsigned long long)ws.d[i];
+    sum = warp_sum(sum);
+    unsigned long long old = 0ull;
+    if (lane == 0)
+        old = atomicAdd(&nxt->qpack, ((unsigned long long)n << p.eb) | sum);
+    old = __shfl_sync(kFull, old, 0);
+    const unsigned long long base = old >> p.eb;
+    unsigned long long run = old & ((1ull << p.eb) - 1ull);
+    int32_t* qv = p.qv[qsel];
+    RowT* qb = p.qbeg[qsel];
+    RowT* qo = p.qoff[qsel];
+    for (int i0 = 0; i0 < n; i0 += 32) {
+        const int i = i0 + lane;
+        const unsigned long long d = i < n ? (unsigned long long)ws.d[i] : 0ull;
+        const unsigned long long inc = warp_inclusive_scan(d);
+        if (i < n) {
+            qv[base + i] = ws.v[i];
+            qb[base + i] = ws.b[i];
+            qo[base + i] = (RowT)(run + inc - d);
+        }
+        run += __shfl_sync(kFull, inc, 31);
+    }
+    __syncwarp();
+}
+
+template <typename RowT>
+__device__ void push_warp_mp(const Params<RowT>& p, int k, int qn, RowT qm, unsigned char* raw,
+                             LevelSlot* nxt, Tally& t, bool pre)
 {
     const int cs = k & 1, ns = cs ^ 1;
     const int32_t* qv = p.qv[cs];
     const RowT* qb = p.qbeg[cs];
     const RowT* qo = p.qoff[cs];
-    const int bd = blockDim.x, lane = threadIdx.x & 31;
-    const unsigned long long G = gridDim.x;
-    const RowT e_lo = (RowT)((unsigned long long)qm * blockIdx.x / G);
-    const RowT e_hi = (RowT)((unsigned long long)qm * (blockIdx.x + 1) / G);
+    const int lane = threadIdx.x & 31;
+    const unsigned long long W = (unsigned long long)gridDim.x * (blockDim.x >> 5);
+    const unsigned long long gw =
+        (unsigned long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    // Edge positions in 64 bits: e + 32 * j never overflows an int32 row_ptr.
+    const long long e_lo = (long long)((unsigned long long)qm * gw / W);
+    const long long e_hi = (long long)((unsigned long long)qm * (gw + 1) / W);
     if (e_lo >= e_hi)
         return;
-    const int tile = bd * kItems;
+    const WarpStage<RowT> ws = warp_stage<RowT>(raw);
 
-    if (threadIdx.x < 32) {
-        // last i in [0, qn) with qoff[i] <= e_lo; qoff[0] = 0 <= e_lo
-        int lo = 0, hi = qn;
-        while (hi - lo > 1) {
-            const int step = (hi - lo + 31) / 32;
-            const int probe = lo + lane * step;
+    // First entry: the last i with qoff[i] <= e_lo (qoff[0] = 0), 32-ary search.
+    int cur = 0;
+    {
+        int hi = qn;
+        while (hi - cur > 1) {
+            const int step = (hi - cur + 31) / 32;
+            const int probe = cur + lane * step;
             const bool le = lane > 0 && probe < hi && ldcg(qo + probe) <= e_lo;
             const unsigned bal = __ballot_sync(kFull, le);
             if (bal == 0u) {
-                hi = min(hi, lo + step);
+                hi = min(hi, cur + step);
             } else {
-                const int top = 31 - __clz(bal);
-                lo = lo + top * step;
-                hi = min(hi, lo + step);
+                cur = cur + (31 - __clz(bal)) * step;
+                hi = min(hi, cur + step);
             }
         }
-        if (lane == 0)
-            ss.cur = lo;
     }
-    __syncthreads();
-
-    // cur: first queue entry the tile touches. The window holds queue entries
-    // [wbase, wbase + wn). Every thread computes both from shared state read
-    // before the end-of-tile barrier, so they are uniform and the window is
-    // only rewritten after every read of it in the previous tile.
-    int cur = ss.cur, wbase = 0, wn = 0;
-    bool covered = false;
-    for (RowT r0 = e_lo; r0 < e_hi; r0 += tile) {
-        const RowT r1 = r0 + (RowT)tile < e_hi ? r0 + (RowT)tile : e_hi;
-        if (!covered) {
-            wbase = cur;
-            wn = min(tile + 1, qn - cur);
-            for (int x = threadIdx.x; x < wn; x += bd) {
-                sm.woff[x] = ldcg(qo + cur + x);
-                sm.wbeg[x] = ldcg(qb + cur + x);
-                sm.wu[x] = ldcg(qv + cur + x);
-            }
-            __syncthreads();
+    RowT off, beg, end;
+    int32_t vtx;
+    // Window of entries [c, c + 32); lanes past the queue hold empty ranges
+    // at m_F.
+    auto load_window = [&](int c) {
+        const int i = c + lane;
+        if (i < qn) {
+            off = ldcg(qo + i);
+            beg = ldcg(qb + i);
+            vtx = ldcg(qv + i);
+        } else {
+            off = qm;
+            beg = 0;
+            vtx = -1;
         }
-        int32_t vv[kItems], uu[kItems];
-        int lo = cur - wbase;
+        RowT nx = __shfl_down_sync(kFull, off, 1);
+        if (lane == 31)
+            nx = c + 32 < qn ? ldcg(qo + c + 32) : qm;
+        end = nx;
+    };
+    load_window(cur);
+    long long e = e_lo;
+    int cnt = 0;  // staged entries (the same in every lane)
+    while (e < e_hi) {
+        const long long wend = (long long)__shfl_sync(kFull, end, 31);
+        if (e >= wend) {  // e is the first edge of entry cur + 32
+            cur += 32;
+            load_window(cur);
+            continue;
+        }
+        const int x0 = __ffs(__ballot_sync(kFull, (long long)end > e)) - 1;
+        int n = 0;
 #pragma unroll
-        for (int it = 0; it < kItems; ++it) {
-            const RowT e = r0 + (RowT)(it * bd + threadIdx.x);
-            vv[it] = -1;
-            uu[it] = 0;
-            if (e < r1) {
-                int hi = wn;
-                while (hi - lo > 1) {
-                    const int mid = (lo + hi) >> 1;
-                    if (sm.woff[mid] <= e)
-                        lo = mid;
-                    else
-                        hi = mid;
+        for (int j = 0; j < kWItems; ++j) {
+            const long long first = e + 32 * j;
+            const long long last = first + 31 < e_hi - 1 ? first + 31 : e_hi - 1;
+            if (n == j && first < e_hi && last < wend)
+                n = j + 1;
+        }
+        if (n < kWItems && x0 > 0 && e + 32 * n < e_hi) {
+            cur += x0;  // slide the window to the entry of e and look again
+            load_window(cur);
+            continue;
+        }
+        if (cnt + 32 * n > kWarpStage) {
+            warp_flush(p, ws, cnt, nxt, ns);
+            cnt = 0;
+        }
+        int32_t vv[kWItems], uu[kWItems];
+#pragma unroll
+        for (int j = 0; j < kWItems; ++j) {
+            vv[j] = -1;
+            uu[j] = 0;
+            if (j < n) {
+                const long long e0 = e + 32 * j;
+                const int xf = __ffs(__ballot_sync(kFull, (long long)end > e0)) - 1;
+                const long long rel = (long long)off - e0;
+                const unsigned starts =
+                    __reduce_or_sync(kFull, (rel > 0 && rel < 32) ? 1u << (int)rel : 0u);
+                const int xl = xf + __popc(starts & ((2u << lane) - 1u));
+                const RowT o = __shfl_sync(kFull, off, xl);
+                const RowT bg = __shfl_sync(kFull, beg, xl);
+                const int32_t u = __shfl_sync(kFull, vtx, xl);
+                const long long ej = e0 + lane;
+                if (ej < e_hi) {
+                    uu[j] = u;
+                    vv[j] = p.col[bg + (RowT)(ej - (long long)o)];
                 }
-                uu[it] = sm.wu[lo];
-                vv[it] = p.col[sm.wbeg[lo] + (e - sm.woff[lo])];
             }
         }
-        bool won[kItems];
+        bool won[kWItems];
         claim_batch(p, k, vv, uu, pre, won);
-        after_win_batch(p, sm, ss, nxt, ns, t, vv, won);
-        if (r1 < e_hi) {
-            // The next tile starts at the last entry with offset <= r1; the
-            // window still serves it when it holds every entry up to the last
-            // one starting before the next tile's end (a frontier of few
-            // high-degree vertices keeps one window for many tiles).
-            int a = cur - wbase, c = wn;
-            while (c - a > 1) {
-                const int mid = (a + c) >> 1;
-                if (sm.woff[mid] <= r1)
-                    a = mid;
-                else
-                    c = mid;
+        RowT wb[kWItems], we[kWItems];
+#pragma unroll
+        for (int j = 0; j < kWItems; ++j) {
+            wb[j] = 0;
+            we[j] = 0;
+            if (won[j]) {
+                wb[j] = p.row_ptr[vv[j]];
+                we[j] = p.row_ptr[vv[j] + 1];
             }
-            cur = wbase + a;
-            const RowT r2 = r1 + (RowT)tile < e_hi ? r1 + (RowT)tile : e_hi;
-            covered = wbase + wn == qn || sm.woff[wn - 1] >= r2;
         }
-        // Flush once the stage is half full (every round when most edges
-        // discover, every few rounds otherwise: fewer global atomics). A round
-        // can add at most TILE entries; any excess is appended directly.
-        if (__syncthreads_or(ss.stage_n > sm.cap / 2))
-            stage_flush(p, sm, ss, nxt, ns);
+#pragma unroll
+        for (int j = 0; j < kWItems; ++j) {
+            const RowT deg = we[j] - wb[j];
+            if (won[j]) {
+                t.found += 1;
+                t.edges += (unsigned long long)deg;
+                t.maxdeg = (unsigned long long)deg > t.maxdeg ? (unsigned long long)deg : t.maxdeg;
+            }
+            const bool take = won[j] && deg > 0;
+            const unsigned m = __ballot_sync(kFull, take);
+            if (take) {
+                const int pos = cnt + __popc(m & ((1u << lane) - 1u));
+                ws.v[pos] = vv[j];
+                ws.b[pos] = wb[j];
+                ws.d[pos] = (int32_t)deg;
+            }
+            cnt += __popc(m);
+        }
+        e += 32 * n;
     }
-    stage_flush(p, sm, ss, nxt, ns);
+    if (cnt > 0)
+        warp_flush(p, ws, cnt, nxt, ns);
 }
 
 // ------------------------------------------------------------ S7 pull level
@@ -1200,9 +1306,10 @@ __device__ void solo_levels(const Params<RowT>& p, int k, int qn, RowT qm, long 
 // ------------------------------------------------------------ kernels
 
 // Dynamic shared memory: the compaction stage (row starts, degrees, vertices)
-// and, after it, one region used either as the merge-path / single-CTA window
+// and, after it, one region used either as the single-CTA levels' frontier
 // (offsets, row starts, vertices) or as the binned advance's CTA-per-vertex
-// list; pull levels reuse the whole buffer for their per-warp lists.
+// list; pull levels reuse the whole buffer for their per-warp lists and the
+// warp-level merge path for its per-warp stages.
 template <typename RowT>
 __device__ __forceinline__ Smem<RowT> carve_smem(unsigned char* raw, int bd)
 {
@@ -1230,7 +1337,9 @@ __host__ __device__ inline size_t level_smem_bytes(int bd)
     const size_t tile = (size_t)bd * kItems;
     const size_t push = (sizeof(RowT) + 8) * tile + (2 * sizeof(RowT) + 4) * (tile + 1) + 16;
     const size_t pull = (size_t)(bd / 32) * (1024 + 32) * sizeof(uint32_t);
-    return push > pull ? push : pull;
+    const size_t wstage = (size_t)(bd / 32) * kWarpStage * (sizeof(RowT) + 8);
+    const size_t m = push > pull ? push : pull;
+    return m > wstage ? m : wstage;
 }
 
 // The persistent level loop (S2-S9).
@@ -1359,7 +1468,7 @@ __global__ void __launch_bounds__(512, 2) level_kernel(Params<RowT> p)
             // costs a round trip otherwise.
             const bool pre = (long long)qm >= 65536 && 2 * U < nonisolated;
             if (adv == BFS_CSR_ADV_MERGE_PATH)
-                push_merge_path(p, k, qn, qm, sm, ss, nxt, t, pre);
+                push_warp_mp(p, k, qn, qm, smem_raw, nxt, t, pre);
             else
                 push_binned(p, k, qn, qm, sm, ss, nxt, t, pre);
         }
