@@ -818,7 +818,8 @@ __device__ void push_warp_mp(const Params<RowT>& p, int k, int qn, RowT qm, unsi
 
 // ------------------------------------------------------------ S7 pull level
 
-constexpr int kPullVerts = 2;    // list entries per lane in flight
+constexpr int kHeadVerts = 4;    // head probes per lane in flight
+constexpr int kPullVerts = 2;    // miss rows per lane in flight
 constexpr int kChunkBatch = 4;   // chunks whose visited words a warp loads together
 constexpr int kPullRounds = 6;   // two-entry probe rounds before the warp takes a row
 
@@ -897,37 +898,55 @@ __device__ void pull_level(const Params<RowT>& p, int k, Tally& t, int32_t* wlis
             }
         }
         __syncwarp();
-        for (int base = 0; base < total; base += 32 * kPullVerts) {
+        // Phase 1: every list entry's probe neighbour, kHeadVerts per lane in
+        // flight. Hits resolve here; a miss with more than one edge is
+        // written back to the front of the list (never past an entry already
+        // read), so phase 2 scans rows for misses only and no lane of a
+        // round idles behind a hit.
+        int nmiss = 0;
+        for (int base = 0; base < total; base += 32 * kHeadVerts) {
+            int32_t hv[kHeadVerts];
+            int2 hd[kHeadVerts];
+            uint32_t hf[kHeadVerts];
+#pragma unroll
+            for (int b = 0; b < kHeadVerts; ++b) {
+                const int j = base + b * 32 + lane;
+                hv[b] = j < total ? wlist[j] : -1;
+                hd[b] = hv[b] >= 0 ? __ldg(p.head + hv[b]) : make_int2(-1, 0);
+            }
+#pragma unroll
+            for (int b = 0; b < kHeadVerts; ++b)
+                hf[b] = hd[b].x >= 0 ? ldcg(fcur + (hd[b].x >> 5)) : 0u;
+            __syncwarp();
+#pragma unroll
+            for (int b = 0; b < kHeadVerts; ++b) {
+                const bool hit = hd[b].x >= 0 && ((hf[b] >> (hd[b].x & 31)) & 1u);
+                if (hit)
+                    pull_resolve(p, k, t, wfound, w0, hv[b], hd[b].x, hd[b].y);
+                const bool miss = hv[b] >= 0 && !hit && hd[b].y > 1;
+                const unsigned mm = __ballot_sync(kFull, miss);
+                if (miss)
+                    wlist[nmiss + __popc(mm & ((1u << lane) - 1u))] = hv[b];
+                nmiss += __popc(mm);
+            }
+            __syncwarp();
+        }
+        // Phase 2: the misses' rows in CSR order, two entries per round.
+        for (int base = 0; base < nmiss; base += 32 * kPullVerts) {
             int32_t v[kPullVerts], par[kPullVerts], deg[kPullVerts];
             RowT cur[kPullVerts], end[kPullVerts];
-            // Round 0: the probe neighbour from the head array (no row_ptr or
-            // col access); only rows that miss it load their offsets and scan
-            // the whole row (a one-entry row has nothing more to scan).
-            {
-                int2 hd[kPullVerts];
 #pragma unroll
-                for (int b = 0; b < kPullVerts; ++b) {
-                    const int j = base + b * 32 + lane;
-                    v[b] = j < total ? wlist[j] : -1;
-                    hd[b] = v[b] >= 0 ? __ldg(p.head + v[b]) : make_int2(-1, 0);
-                }
-                uint32_t f0[kPullVerts];
-#pragma unroll
-                for (int b = 0; b < kPullVerts; ++b)
-                    f0[b] = hd[b].x >= 0 ? ldcg(fcur + (hd[b].x >> 5)) : 0u;
-#pragma unroll
-                for (int b = 0; b < kPullVerts; ++b) {
-                    deg[b] = hd[b].y;
-                    par[b] = (hd[b].x >= 0 && ((f0[b] >> (hd[b].x & 31)) & 1u)) ? hd[b].x : -1;
-                    cur[b] = 0;
-                    end[b] = 0;
-                }
-#pragma unroll
-                for (int b = 0; b < kPullVerts; ++b) {
-                    if (v[b] >= 0 && par[b] < 0 && deg[b] > 1) {
-                        cur[b] = p.row_ptr[v[b]];
-                        end[b] = cur[b] + (RowT)deg[b];
-                    }
+            for (int b = 0; b < kPullVerts; ++b) {
+                const int j = base + b * 32 + lane;
+                v[b] = j < nmiss ? wlist[j] : -1;
+                par[b] = -1;
+                cur[b] = 0;
+                end[b] = 0;
+                deg[b] = 0;
+                if (v[b] >= 0) {
+                    cur[b] = p.row_ptr[v[b]];
+                    end[b] = p.row_ptr[v[b] + 1];
+                    deg[b] = (int32_t)(end[b] - cur[b]);
                 }
             }
             for (int round = 0; round < kPullRounds; ++round) {
