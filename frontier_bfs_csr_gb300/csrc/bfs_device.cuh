@@ -1398,8 +1398,23 @@ __global__ void __launch_bounds__(512, 2) level_kernel(Params<RowT> p)
         if (F == 0 || (p.max_depth >= 0 && k >= p.max_depth)) {
             if (leader) {
                 const int nl = F == 0 ? k : k + 1;
+                const unsigned long long t_end = global_timer_ns();
+                if (F != 0 && k < p.stats_cap) {
+                    // Depth bound: F_k counts as a level but is not expanded.
+                    bfs_csr_level_stat st;
+                    st.level = k;
+                    st.direction = 0;
+                    st.advance = 0;
+                    st.reserved = 0;
+                    st.frontier = F;
+                    st.frontier_edges = (long long)fedges;
+                    st.unvisited = uprev - F;
+                    st.max_degree = (long long)maxdeg;
+                    st.t_start_ns = (long long)t_end;
+                    p.stats[k] = st;
+                }
                 p.ctl->num_levels = nl;
-                p.ctl->t_end_ns = global_timer_ns();
+                p.ctl->t_end_ns = t_end;
                 if (p.num_levels_out != nullptr)
                     *p.num_levels_out = nl;
                 __threadfence();

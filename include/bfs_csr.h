@@ -93,8 +93,11 @@ typedef struct bfs_csr_options {
 /* Per-level record, kept when the run completes (see bfs_csr_level_stats). */
 typedef struct bfs_csr_level_stat {
     int32_t level;           /* k: the frontier holds the vertices at distance k */
-    int32_t direction;       /* BFS_CSR_DIR_PUSH or BFS_CSR_DIR_PULL */
-    int32_t advance;         /* push levels: BFS_CSR_ADV_BINNED or _MERGE_PATH */
+    int32_t direction;       /* BFS_CSR_DIR_PUSH or BFS_CSR_DIR_PULL; 0 for the
+                                last frontier of a run cut by max_depth, which
+                                counts as a level but is not expanded */
+    int32_t advance;         /* push levels: BFS_CSR_ADV_BINNED, _MERGE_PATH or
+                                _SINGLE_CTA; 0 otherwise */
     int32_t reserved;
     int64_t frontier;        /* |F_k| */
     int64_t frontier_edges;  /* m_F: sum of out-degrees over F_k */

@@ -226,6 +226,27 @@ def test_option_matrix(fbc, over):
         bfs.close()
 
 
+@pytest.mark.parametrize("depth", [0, 1, 2, 3, 5])
+def test_depth_bound_with_level_records(fbc, depth):
+    """max_depth = d: dist matches the oracle's depth-bounded search, the
+    level count includes the last (unexpanded) frontier F_d, and its record
+    has direction 0 and the right size."""
+    for cfg in (1, 3):
+        g = graphgen.config(cfg)
+        for over in (dict(), dict(direction=1), dict(narrow_max_edges=0)):
+            opt = fbc.default_options(max_depth=depth, **over)
+            bfs = fbc.BfsCsr(_dev(g.row_ptr), _dev(g.col), True, opt)
+            check_against_oracle(fbc, g, g.sources[:2], bfs=bfs, max_depth=depth)
+            rec = bfs.level_stats()
+            want, _, levels = oracle.bfs(g.row_ptr, g.col, int(g.sources[1]), max_depth=depth,
+                                         want_parent=False)
+            if levels == depth + 1:
+                assert rec[-1]["direction"] == 0 and rec[-1]["level"] == depth
+                assert rec[-1]["frontier"] == int((want == depth).sum())
+            assert all(r["direction"] in (1, 2) for r in rec[:levels - 1])
+            bfs.close()
+
+
 def test_stage_overflow_path(fbc):
     """One CTA, binned advance: a level where 3,000 frontier vertices each
     discover 20 new leaves overflows the shared-memory stage; the overflow
