@@ -43,7 +43,7 @@ EXPORTED = [
     "bfs_csr_default_options", "bfs_csr_workspace_bytes", "bfs_csr_create", "bfs_csr_run",
     "bfs_csr_run_init", "bfs_csr_run_levels",
     "bfs_csr_sync", "bfs_csr_level_stats", "bfs_csr_create_host", "bfs_csr_run_host",
-    "bfs_csr_destroy", "bfs_csr_status_string", "bfs_csr_last_cuda_error",
+    "bfs_csr_run_host_batch", "bfs_csr_destroy", "bfs_csr_status_string", "bfs_csr_last_cuda_error",
     "bfs_csr_run_noalloc",
 ]
 BFS_CSR_NOALLOC_MAX_VERTICES = 1048576
@@ -102,6 +102,7 @@ _sig = {
     "bfs_csr_create_host": ([ctypes.POINTER(_vp), _i64, _i64, _vp, _i32, _vp, _i32, _opt_p, _vp],
                             _i32),
     "bfs_csr_run_host": ([_vp, _i64, _vp, _vp, _vp, _vp, _vp, _vp], _i32),
+    "bfs_csr_run_host_batch": ([_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp], _i32),
     "bfs_csr_destroy": ([_vp], _i32),
     "bfs_csr_status_string": ([_i32], ctypes.c_char_p),
     "bfs_csr_last_cuda_error": ([_vp], _i32),
@@ -287,6 +288,30 @@ class BfsCsrHost:
                                   ctypes.addressof(levels), _stream_ptr(stream))
         _check(status, "bfs_csr_run_host", self.handle)
         return int(levels.value)
+
+    def run_batch(self, sources, dist, parent=None, levels=None, row_ptr=None, col=None,
+                  stream=None) -> None:
+        """Search from every source; row i of dist (and parent) is source i's
+        result. dist/parent: C-contiguous int32 arrays of len(sources) x n
+        (pinned for asynchronous copies); levels: int32 array of len(sources)
+        or None. row_ptr/col re-upload the CSR first, as in :meth:`run`."""
+        import numpy as np
+        src = np.ascontiguousarray(np.asarray(sources, dtype=np.int64))
+        k = int(src.shape[0])
+        for a in (dist, parent):
+            if a is not None and (a.dtype != np.int32 or a.size != k * self.n or
+                                  not a.flags["C_CONTIGUOUS"]):
+                raise ValueError("dist/parent must be C-contiguous int32 of len(sources) x n")
+        if levels is not None and (levels.dtype != np.int32 or levels.size != k):
+            raise ValueError("levels must be int32 of len(sources)")
+        status = bfs_csr_run_host_batch(self.handle, k, src.ctypes.data,
+                                        row_ptr.ctypes.data if row_ptr is not None else None,
+                                        col.ctypes.data if col is not None else None,
+                                        dist.ctypes.data,
+                                        parent.ctypes.data if parent is not None else None,
+                                        levels.ctypes.data if levels is not None else None,
+                                        _stream_ptr(stream))
+        _check(status, "bfs_csr_run_host_batch", self.handle)
 
     def close(self) -> None:
         if getattr(self, "handle", None):

@@ -12,6 +12,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <vector>
 #include <new>
 
 #include "bfs_csr.h"
@@ -93,6 +94,15 @@ struct bfs_csr_t {
     int32_t* d_dist_own = nullptr;
     int32_t* d_parent_own = nullptr;
     int32_t* d_levels_own = nullptr;
+    // host-memory batches: a second output slot, per-search level counts and
+    // end states, and a copy stream with its events (made on first use)
+    int32_t* d_dist_b = nullptr;
+    int32_t* d_parent_b = nullptr;
+    int32_t* d_batch = nullptr;   // per search: status, done, level, num_levels
+    int32_t batch_cap = 0;
+    cudaStream_t copy_stream = nullptr;
+    cudaEvent_t ev_search[2] = {nullptr, nullptr};
+    cudaEvent_t ev_copy[2] = {nullptr, nullptr};
 };
 
 namespace {
@@ -325,6 +335,14 @@ void release(bfs_csr_t* h)
     if (h->d_dist_own) cudaFree(h->d_dist_own);
     if (h->d_parent_own) cudaFree(h->d_parent_own);
     if (h->d_levels_own) cudaFree(h->d_levels_own);
+    if (h->d_dist_b) cudaFree(h->d_dist_b);
+    if (h->d_parent_b) cudaFree(h->d_parent_b);
+    if (h->d_batch) cudaFree(h->d_batch);
+    for (int i = 0; i < 2; ++i) {
+        if (h->ev_search[i]) cudaEventDestroy(h->ev_search[i]);
+        if (h->ev_copy[i]) cudaEventDestroy(h->ev_copy[i]);
+    }
+    if (h->copy_stream) cudaStreamDestroy(h->copy_stream);
     delete h;
 }
 
@@ -347,6 +365,20 @@ int init_handle(bfs_csr_t* h, int64_t n, int64_t nnz, int row_ptr_64, int symmet
     if (!coop)
         return BFS_CSR_EUNSUPPORTED;
     return BFS_CSR_OK;
+}
+
+// Host CSR -> the handle's device copy (same n and nnz), then the checks and
+// per-vertex data create derives from it.
+int upload_host_csr(bfs_csr_t* h, const void* h_row_ptr, const int32_t* h_col, cudaStream_t s)
+{
+    const size_t rp_bytes = (size_t)(h->n + 1) * (h->row_ptr_64 ? 8 : 4);
+    FBC_CUDA(h, cudaMemcpyAsync(h->d_row_ptr_own, h_row_ptr, rp_bytes, cudaMemcpyHostToDevice, s));
+    if (h->nnz > 0)
+        FBC_CUDA(h, cudaMemcpyAsync(h->d_col_own, h_col, (size_t)h->nnz * 4,
+                                    cudaMemcpyHostToDevice, s));
+    // A new CSR: validate it and re-derive the dead bitmap, the non-isolated
+    // count and the head array, as create does.
+    return h->row_ptr_64 ? prepare<int64_t>(h, s) : prepare<int32_t>(h, s);
 }
 
 }  // namespace
@@ -560,14 +592,7 @@ int bfs_csr_run_host(bfs_csr_handle h, int64_t source, const void* h_row_ptr, co
         return BFS_CSR_EINVAL;
     cudaStream_t s = as_stream(stream);
     if (h_row_ptr != nullptr) {
-        const size_t rp_bytes = (size_t)(h->n + 1) * (h->row_ptr_64 ? 8 : 4);
-        FBC_CUDA(h, cudaMemcpyAsync(h->d_row_ptr_own, h_row_ptr, rp_bytes, cudaMemcpyHostToDevice, s));
-        if (h->nnz > 0)
-            FBC_CUDA(h, cudaMemcpyAsync(h->d_col_own, h_col, (size_t)h->nnz * 4,
-                                        cudaMemcpyHostToDevice, s));
-        // A new CSR: validate it and re-derive the dead bitmap, the
-        // non-isolated count and the head array, as create does.
-        const int prc = h->row_ptr_64 ? prepare<int64_t>(h, s) : prepare<int32_t>(h, s);
+        const int prc = upload_host_csr(h, h_row_ptr, h_col, s);
         if (prc != BFS_CSR_OK)
             return prc;
     }
@@ -584,6 +609,94 @@ int bfs_csr_run_host(bfs_csr_handle h, int64_t source, const void* h_row_ptr, co
     if (h_num_levels != nullptr)
         *h_num_levels = levels;
     return rc;
+}
+
+int bfs_csr_run_host_batch(bfs_csr_handle h, int32_t num_sources, const int64_t* sources,
+                           const void* h_row_ptr, const int32_t* h_col, int32_t* h_dist,
+                           int32_t* h_parent, int32_t* h_num_levels, void* stream)
+{
+    if (h == nullptr || !h->host_mode || num_sources <= 0 || sources == nullptr ||
+        h_dist == nullptr)
+        return BFS_CSR_EINVAL;
+    if (h_row_ptr == nullptr && h_col != nullptr)
+        return BFS_CSR_EINVAL;
+    if (h_row_ptr != nullptr && h->nnz > 0 && h_col == nullptr)
+        return BFS_CSR_EINVAL;
+    for (int32_t i = 0; i < num_sources; ++i)
+        if (sources[i] < 0 || sources[i] >= h->n)
+            return BFS_CSR_EINVAL;
+    cudaStream_t s = as_stream(stream);
+    const size_t out_bytes = (size_t)h->n * 4;
+    // First batch: the second output slot, the copy stream and its events.
+    if (h->copy_stream == nullptr) {
+        FBC_CUDA(h, cudaMalloc(&h->d_dist_b, out_bytes));
+        FBC_CUDA(h, cudaMalloc(&h->d_parent_b, out_bytes));
+        FBC_CUDA(h, cudaStreamCreateWithFlags(&h->copy_stream, cudaStreamNonBlocking));
+        for (int i = 0; i < 2; ++i) {
+            FBC_CUDA(h, cudaEventCreateWithFlags(&h->ev_search[i], cudaEventDisableTiming));
+            FBC_CUDA(h, cudaEventCreateWithFlags(&h->ev_copy[i], cudaEventDisableTiming));
+        }
+    }
+    if (num_sources > h->batch_cap) {
+        if (h->d_batch != nullptr) {
+            FBC_CUDA(h, cudaFree(h->d_batch));
+            h->d_batch = nullptr;
+            h->batch_cap = 0;
+        }
+        FBC_CUDA(h, cudaMalloc(&h->d_batch, (size_t)num_sources * 4 * sizeof(int32_t)));
+        h->batch_cap = num_sources;
+    }
+    if (h_row_ptr != nullptr) {
+        const int prc = upload_host_csr(h, h_row_ptr, h_col, s);
+        if (prc != BFS_CSR_OK)
+            return prc;
+    }
+    int32_t* slot_dist[2] = {h->d_dist_own, h->d_dist_b};
+    int32_t* slot_parent[2] = {h->d_parent_own, h->d_parent_b};
+    const Ctl* ctl = reinterpret_cast<const Ctl*>(h->ws + h->L.ctl);
+    cudaStream_t cs = h->copy_stream;
+    // Search i writes slot i % 2 on `stream`; its copy-back runs on the copy
+    // stream while search i + 1 runs, and search i + 2 waits for it.
+    for (int32_t i = 0; i < num_sources; ++i) {
+        const int sl = i & 1;
+        if (i >= 2)
+            FBC_CUDA(h, cudaStreamWaitEvent(s, h->ev_copy[sl], 0));
+        const int rc = bfs_csr_run(h, sources[i], slot_dist[sl],
+                                   h_parent != nullptr ? slot_parent[sl] : nullptr, nullptr, s);
+        if (rc != BFS_CSR_OK) {
+            cudaStreamSynchronize(s);
+            cudaStreamSynchronize(cs);
+            return rc;
+        }
+        // The run's end state (status, done, level, level count) for the check below.
+        FBC_CUDA(h, cudaMemcpyAsync(h->d_batch + 4 * i, &ctl->status, 4 * sizeof(int32_t),
+                                    cudaMemcpyDeviceToDevice, s));
+        FBC_CUDA(h, cudaEventRecord(h->ev_search[sl], s));
+        FBC_CUDA(h, cudaStreamWaitEvent(cs, h->ev_search[sl], 0));
+        FBC_CUDA(h, cudaMemcpyAsync(h_dist + (size_t)i * h->n, slot_dist[sl], out_bytes,
+                                    cudaMemcpyDeviceToHost, cs));
+        if (h_parent != nullptr)
+            FBC_CUDA(h, cudaMemcpyAsync(h_parent + (size_t)i * h->n, slot_parent[sl], out_bytes,
+                                        cudaMemcpyDeviceToHost, cs));
+        FBC_CUDA(h, cudaEventRecord(h->ev_copy[sl], cs));
+    }
+    std::vector<int32_t> st((size_t)num_sources * 4);
+    FBC_CUDA(h, cudaMemcpyAsync(st.data(), h->d_batch, st.size() * sizeof(int32_t),
+                                cudaMemcpyDeviceToHost, s));
+    FBC_CUDA(h, cudaStreamSynchronize(s));
+    FBC_CUDA(h, cudaStreamSynchronize(cs));
+    int first_bad = BFS_CSR_OK;
+    for (int32_t i = 0; i < num_sources; ++i) {
+        const int status = st[4 * i], done = st[4 * i + 1];
+        if (h_num_levels != nullptr)
+            h_num_levels[i] = st[4 * i + 3];
+        const int r = status != BFS_CSR_OK ? status : (done == 0 ? BFS_CSR_EDEVICE : BFS_CSR_OK);
+        if (r != BFS_CSR_OK && first_bad == BFS_CSR_OK)
+            first_bad = r;
+    }
+    h->last_status = st[4 * (num_sources - 1)];
+    h->last_num_levels = st[4 * (num_sources - 1) + 3];
+    return first_bad;
 }
 
 int bfs_csr_destroy(bfs_csr_handle h)

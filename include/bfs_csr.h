@@ -193,6 +193,25 @@ int bfs_csr_run_host(bfs_csr_handle h, int64_t source, const void *h_row_ptr,
                      const int32_t *h_col, int32_t *h_dist, int32_t *h_parent,
                      int32_t *h_num_levels, void *stream);
 
+/*
+ * Host-memory batch: one call searches from every source of sources[0 ..
+ * num_sources) on a bfs_csr_create_host handle. When h_row_ptr/h_col are
+ * non-NULL the CSR is first re-uploaded and re-derived as in
+ * bfs_csr_run_host. Search i writes row i of h_dist (and of h_parent when it
+ * is non-NULL): num_sources x n int32, row-major, caller-owned host memory
+ * (pinned, so that the copies run asynchronously). The copy-back of search i
+ * overlaps search i + 1: the handle keeps two device output slots and a copy
+ * stream (allocated on the first call: 8n bytes more). h_num_levels
+ * (num_sources int32, may be NULL) receives each search's level count. The
+ * call synchronises before returning and returns the first failing search's
+ * status, BFS_CSR_OK when all succeeded. BFS_CSR_EINVAL for a NULL argument,
+ * num_sources <= 0 or a source outside [0, n); nothing runs then.
+ */
+int bfs_csr_run_host_batch(bfs_csr_handle h, int32_t num_sources, const int64_t *sources,
+                           const void *h_row_ptr, const int32_t *h_col,
+                           int32_t *h_dist, int32_t *h_parent, int32_t *h_num_levels,
+                           void *stream);
+
 /* Release everything the library allocated for the handle. */
 int bfs_csr_destroy(bfs_csr_handle h);
 

@@ -358,6 +358,37 @@ def test_host_memory_api(fbc):
     h.close()
 
 
+def test_host_memory_batch(fbc):
+    """bfs_csr_run_host_batch: row i of the outputs is source i's search (odd
+    and even batch sizes exercise both output slots), with and without a CSR
+    re-upload, parent and level counts; bad arguments run nothing."""
+    for cfg in (1, 3):
+        g = graphgen.config(cfg)
+        h = fbc.BfsCsrHost(g.row_ptr, g.col, True)
+        for k in (1, 2, 3, 5):
+            srcs = [int(x) for x in g.sources[:k]][::-1]
+            dist = np.full((k, g.n), -7, np.int32)
+            par = np.full((k, g.n), -7, np.int32)
+            lev = np.zeros(k, np.int32)
+            up = k == 3
+            h.run_batch(srcs, dist, par, lev, row_ptr=g.row_ptr if up else None,
+                        col=g.col if up else None)
+            for i, s in enumerate(srcs):
+                want, _, want_levels = oracle.bfs(g.row_ptr, g.col, s, want_parent=False)
+                assert np.array_equal(dist[i], want), (cfg, k, i)
+                assert lev[i] == want_levels
+                assert oracle.check_parent(g.row_ptr, g.col, s, dist[i], par[i])[0] == 0
+        dist = np.empty((2, g.n), np.int32)
+        h.run_batch(g.sources[:2], dist)
+        for i in range(2):
+            want, _, _ = oracle.bfs(g.row_ptr, g.col, int(g.sources[i]), want_parent=False)
+            assert np.array_equal(dist[i], want)
+        for bad in ([], [g.n], [-1]):
+            with pytest.raises(fbc.BfsError):
+                h.run_batch(bad, np.empty((len(bad), g.n), np.int32))
+        h.close()
+
+
 def test_host_memory_api_new_csr_of_the_same_size(fbc):
     """Each upload of a different CSR with the same n and nnz is searched as
     that graph: the degree-0 bitmap and the head array are re-derived."""
