@@ -141,7 +141,10 @@ def algorithmic_bytes(torch, row_ptr, col, deg, src_of_edge, dist, stats, row_by
     row offsets 2R |U'_k|, col 4 c_k, one frontier-bitmap word per scanned
     entry 4 c_k, dist and parent 8 |N_k|, next-frontier bitmap n/8, visited
     words with a discovery 4 per word. Representation switches: queue to bitmap
-    n/8 + 8 |Q_k|; bitmap to queue n/8 + 2R |F_k| + (4 + 2R) |Q_k|.
+    n/8 + 8 |Q_k|; bitmap to queue n/8 + 2R |F_k| + (4 + 2R) |Q_k|. Output:
+    the -1 of every unreached vertex's dist, 4 (n - reached), written by the
+    level kernel when the search ends (the reached vertices' dist bytes are
+    counted at their discovery above).
     """
     n = int(dist.numel())
     R = row_bytes
@@ -191,12 +194,15 @@ def algorithmic_bytes(torch, row_ptr, col, deg, src_of_edge, dist, stats, row_by
         per_level.append(b)
         total += b
         prev = st["direction"]
+    total += 4 * int((dist < 0).sum().item())
     return total, per_level
 
 
 def init_bytes(n: int, with_parent: bool = True) -> int:
+    """The init kernel with bitmap discovery: one hop-code byte per vertex,
+    parent (-1), the visited bitmap written and the dead bitmap read."""
     words = (n + 31) // 32
-    return 4 * n + (4 * n if with_parent else 0) + 8 * words
+    return (n + 15) // 16 * 16 + (4 * n if with_parent else 0) + 8 * words
 
 
 # ------------------------------------------------------------------ distributed

@@ -27,7 +27,7 @@ constexpr int kStatsCap = 1 << 16;
 constexpr int kDefaultBlock = 512;
 
 struct Layout {
-    size_t ctl, visited, dead, head, fb0, fb1, qv0, qv1, qbeg0, qbeg1, qoff0, qoff1, stats, total;
+    size_t ctl, visited, dead, head, hop, fb0, fb1, qv0, qv1, qbeg0, qbeg1, qoff0, qoff1, stats, total;
 };
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -47,6 +47,7 @@ Layout make_layout(int64_t n, int row_ptr_64)
     L.visited = take(words * 4);
     L.dead = take(words * 4);
     L.head = take((size_t)n * 8);
+    L.hop = take(align_up((size_t)n, 16));
     L.fb0 = take(words * 4);
     L.fb1 = take(words * 4);
     L.qv0 = take((size_t)n * 4);
@@ -188,6 +189,8 @@ Params<RowT> make_params(bfs_csr_t* h, int32_t* d_dist, int32_t* d_parent, int32
     p.visited = reinterpret_cast<uint32_t*>(w + h->L.visited);
     p.dead = reinterpret_cast<const uint32_t*>(w + h->L.dead);
     p.head = reinterpret_cast<const int2*>(w + h->L.head);
+    p.hop = reinterpret_cast<uint8_t*>(w + h->L.hop);
+    p.defer_dist = h->opt.discovery == BFS_CSR_DISC_BITMAP ? 1 : 0;
     p.vec_out = ((reinterpret_cast<uintptr_t>(d_dist) & 15u) == 0 &&
                  (reinterpret_cast<uintptr_t>(d_parent) & 15u) == 0) ? 1 : 0;
     p.fb[0] = reinterpret_cast<uint32_t*>(w + h->L.fb0);
@@ -741,7 +744,7 @@ constexpr int64_t kNoAllocMaxN = BFS_CSR_NOALLOC_MAX_VERTICES;
 // to 256 bytes.
 constexpr size_t kNoAllocBytes =
     (sizeof(Ctl) + 256) + 4 * ((size_t)kNoAllocMaxN / 8 + 256) +
-    ((size_t)kNoAllocMaxN * 8 + 256) +
+    ((size_t)kNoAllocMaxN * 8 + 256) + ((size_t)kNoAllocMaxN + 256) +
     2 * ((size_t)kNoAllocMaxN * 4 + 256) + 4 * ((size_t)kNoAllocMaxN * 4 + 256) +
     ((size_t)kStatsCap * sizeof(bfs_csr_level_stat) + 256);
 

@@ -93,6 +93,12 @@ struct Params {
     int32_t words;              // ceil(n / 32)
     int32_t* dist;
     int32_t* parent;            // may be null
+    // Hop code per vertex while a search runs (bitmap discovery only): 0
+    // unreached, d + 1 for a distance d < kHopDirect, kHopFar when the
+    // distance itself went straight to dist. dist is written from it once,
+    // coalesced, when the search ends.
+    uint8_t* hop;
+    int defer_dist;             // 1: discoveries write hop, not dist
     uint32_t* visited;
     const uint32_t* dead;       // degree-0 vertices and padding bits (symmetric CSR)
     const int2* head;           // per vertex: (first neighbour or -1, degree)
@@ -400,6 +406,29 @@ __device__ void publish_tally(const Tally& t, LevelSlot* nxt, SmemScalars& ss)
 
 // ------------------------------------------------------------ S5 discovery
 
+// Distances below kHopDirect are kept as one byte per vertex during the
+// search: a discovery then touches one byte of an array an eighth the size
+// of dist (it mostly stays in L2) instead of a 4-byte slot of a 32-byte DRAM
+// sector that must be read, merged and written back. Larger distances (long
+// paths, lattices) go to dist directly and are marked kHopFar.
+constexpr int kHopDirect = 254;
+constexpr uint8_t kHopFar = 255;
+
+template <typename RowT>
+__device__ __forceinline__ void record_dist(const Params<RowT>& p, int32_t v, int d)
+{
+    if (p.defer_dist) {
+        if (d < kHopDirect) {
+            p.hop[v] = (uint8_t)(d + 1);
+        } else {
+            p.hop[v] = kHopFar;
+            p.dist[v] = d;
+        }
+    } else {
+        p.dist[v] = d;
+    }
+}
+
 // The claim of vertex v by frontier vertex u at level k. Exactly one caller
 // per v gets true; the winner writes dist[v] and parent[v].
 template <typename RowT>
@@ -419,7 +448,7 @@ __device__ __forceinline__ bool claim(const Params<RowT>& p, int k, int32_t v, i
             return false;
         if (atomicOr(w, bit) & bit)
             return false;
-        p.dist[v] = k + 1;
+        record_dist(p, v, k + 1);
     }
     if (p.parent != nullptr)
         p.parent[v] = u;
@@ -462,7 +491,7 @@ __device__ __forceinline__ void claim_batch(const Params<RowT>& p, int k, const 
         for (int i = 0; i < N; ++i) {
             won[i] = v[i] >= 0 && !(old[i] & (1u << (v[i] & 31)));
             if (won[i])
-                p.dist[v[i]] = k + 1;
+                record_dist(p, v[i], k + 1);
         }
     }
     if (p.parent != nullptr) {
@@ -820,33 +849,39 @@ __device__ void push_warp_mp(const Params<RowT>& p, int k, int qn, RowT qm, unsi
 
 constexpr int kHeadVerts = 4;    // head probes per lane in flight
 constexpr int kPullVerts = 2;    // miss rows per lane in flight
-constexpr int kChunkBatch = 4;   // chunks whose visited words a warp loads together
 constexpr int kPullRounds = 6;   // two-entry probe rounds before the warp takes a row
+constexpr int kPullList = 1024;  // per-warp list of unvisited vertices
+constexpr int kPullWin = 128;    // visited-bitmap words per warp window (4,096 vertices)
 
 // Pull level over the frontier bitmap fb[k & 1] (bit u set iff u is in F_k).
-// A warp owns a chunk of up to 32 visited-bitmap words (up to 1,024 vertices;
-// fewer on small graphs, so that every warp gets chunks): it first compacts
-// the chunk's unvisited vertices into a per-warp list in shared memory, then
-// each lane takes kPullVerts list entries at once (independent chains of
-// head -> frontier-bitmap loads, so their latencies overlap). The first test
-// is the probe neighbour stored in the head array (read nearly sequentially,
-// with the degree); most rows found by a wide pull level resolve there and
-// never touch row_ptr or col. A row that misses is scanned in CSR order, two
-// entries per round; one still unresolved after kPullRounds rounds is scanned
-// by the whole warp, 32 entries per step, and the lowest hitting lane gives
-// the first frontier neighbour in CSR order, as the per-lane scan does. The
-// parent is thus the probe neighbour when it is in F_k, else the first
-// neighbour in F_k in CSR order. The warp is the only
-// writer of its chunk's visited and next-frontier words, so no global atomics
-// are needed, and every next-frontier word is written, so that bitmap needs
-// no clearing.
+// Every warp owns a contiguous range of visited-bitmap words and walks it in
+// windows of kPullWin words: it stages the window's visited words in shared
+// memory, compacts the unvisited vertices into a per-warp list (processing
+// the list whenever the next 32 words would overflow it), and at the window's
+// end writes the window's visited and next-frontier words. A sparse level
+// (few unvisited vertices) thus costs one list pass per window, not one per
+// 32 words.
+//
+// A list pass (pull_list) first tests, for every entry, the probe neighbour
+// stored in the head array (read nearly sequentially, with the degree;
+// kHeadVerts entries per lane in flight, so their head -> frontier-bitmap
+// chains overlap); most rows found by a wide pull level resolve there and
+// never touch row_ptr or col. Rows that miss are scanned in CSR order, two
+// entries per round and kPullVerts rows per lane; one still unresolved after
+// kPullRounds rounds is scanned by the whole warp, 32 entries per step, and
+// the lowest hitting lane gives the first frontier neighbour in CSR order, as
+// the per-lane scan does. The parent is thus the probe neighbour when it is
+// in F_k, else the first neighbour in F_k in CSR order. The warp is the only
+// writer of its words of the visited and next-frontier bitmaps, so no global
+// atomics are needed, and every next-frontier word is written, so that bitmap
+// needs no clearing.
 
 template <typename RowT>
 __device__ __forceinline__ void pull_resolve(const Params<RowT>& p, int k, Tally& t,
                                              uint32_t* wfound, int w0, int32_t x, int32_t par,
                                              int32_t deg)
 {
-    p.dist[x] = k + 1;
+    record_dist(p, x, k + 1);
     if (p.parent != nullptr)
         p.parent[x] = par;
     atomicOr(&wfound[(x >> 5) - w0], 1u << (x & 31));
@@ -855,182 +890,206 @@ __device__ __forceinline__ void pull_resolve(const Params<RowT>& p, int k, Tally
     t.maxdeg = (unsigned long long)deg > t.maxdeg ? (unsigned long long)deg : t.maxdeg;
 }
 
+// One pass over the warp's list wlist[0, total) of unvisited vertices, all in
+// the window whose first visited-bitmap word is w0: phase 1 (head probes)
+// then phase 2 (row scans of the misses). Found vertices get their bit in
+// wfound (indexed by word - w0).
 template <typename RowT>
-__device__ void pull_level(const Params<RowT>& p, int k, Tally& t, int32_t* wlist,
-                           uint32_t* wfound)
+__device__ void pull_list(const Params<RowT>& p, int k, Tally& t, int32_t* wlist, int total,
+                          uint32_t* wfound, int w0)
 {
     const uint32_t* fcur = p.fb[k & 1];
-    uint32_t* fnext = p.fb[(k + 1) & 1];
     const int lane = threadIdx.x & 31;
-    const int gwarp = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
-    const int nwarps = (int)((gridDim.x * blockDim.x) >> 5);
-    int cw = (p.words + 4 * nwarps - 1) / (4 * nwarps);  // words per chunk
-    cw = cw < 1 ? 1 : (cw > 32 ? 32 : cw);
-    const int nchunks = (p.words + cw - 1) / cw;
-    // Chunks c = gwarp + i * nwarps; the visited words of kChunkBatch of them
-    // are loaded together.
-    for (int cb = gwarp; cb < nchunks; cb += kChunkBatch * nwarps) {
-      uint32_t visb[kChunkBatch];
+    // Phase 1: every list entry's probe neighbour, kHeadVerts per lane in
+    // flight. Hits resolve here; a miss with more than one edge is
+    // written back to the front of the list (never past an entry already
+    // read), so phase 2 scans rows for misses only and no lane of a
+    // round idles behind a hit.
+    int nmiss = 0;
+    for (int base = 0; base < total; base += 32 * kHeadVerts) {
+        int32_t hv[kHeadVerts];
+        int2 hd[kHeadVerts];
+        uint32_t hf[kHeadVerts];
 #pragma unroll
-      for (int i = 0; i < kChunkBatch; ++i) {
-          const int ci = cb + i * nwarps;
-          const int wi = ci * cw + lane;
-          visb[i] = (ci < nchunks && lane < cw && wi < p.words) ? ldcg(p.visited + wi) : kFull;
-      }
-#pragma unroll 1
-      for (int i = 0; i < kChunkBatch && cb + i * nwarps < nchunks; ++i) {
-        const int c = cb + i * nwarps;
-        const int w0 = c * cw;
-        const int w = w0 + lane;
-        const uint32_t vis = visb[i];
-        const uint32_t todo = ~vis;
-        const int cnt = __popc(todo);
-        const int incl = warp_inclusive_scan(cnt);
-        const int total = __shfl_sync(kFull, incl, 31);
-        wfound[lane] = 0u;
-        if (total > 0) {
-            int pos = incl - cnt;
-            uint32_t m = todo;
-            while (m) {
-                const int b = __ffs(m) - 1;
-                m &= m - 1;
-                wlist[pos++] = (w << 5) + b;
-            }
+        for (int b = 0; b < kHeadVerts; ++b) {
+            const int j = base + b * 32 + lane;
+            hv[b] = j < total ? wlist[j] : -1;
+            hd[b] = hv[b] >= 0 ? __ldg(p.head + hv[b]) : make_int2(-1, 0);
+        }
+#pragma unroll
+        for (int b = 0; b < kHeadVerts; ++b)
+            hf[b] = hd[b].x >= 0 ? ldcg(fcur + (hd[b].x >> 5)) : 0u;
+        __syncwarp();
+#pragma unroll
+        for (int b = 0; b < kHeadVerts; ++b) {
+            const bool hit = hd[b].x >= 0 && ((hf[b] >> (hd[b].x & 31)) & 1u);
+            if (hit)
+                pull_resolve(p, k, t, wfound, w0, hv[b], hd[b].x, hd[b].y);
+            const bool miss = hv[b] >= 0 && !hit && hd[b].y > 1;
+            const unsigned mm = __ballot_sync(kFull, miss);
+            if (miss)
+                wlist[nmiss + __popc(mm & ((1u << lane) - 1u))] = hv[b];
+            nmiss += __popc(mm);
         }
         __syncwarp();
-        // Phase 1: every list entry's probe neighbour, kHeadVerts per lane in
-        // flight. Hits resolve here; a miss with more than one edge is
-        // written back to the front of the list (never past an entry already
-        // read), so phase 2 scans rows for misses only and no lane of a
-        // round idles behind a hit.
-        int nmiss = 0;
-        for (int base = 0; base < total; base += 32 * kHeadVerts) {
-            int32_t hv[kHeadVerts];
-            int2 hd[kHeadVerts];
-            uint32_t hf[kHeadVerts];
+    }
+    // Phase 2: the misses' rows in CSR order, two entries per round.
+    for (int base = 0; base < nmiss; base += 32 * kPullVerts) {
+        int32_t v[kPullVerts], par[kPullVerts], deg[kPullVerts];
+        RowT cur[kPullVerts], end[kPullVerts];
 #pragma unroll
-            for (int b = 0; b < kHeadVerts; ++b) {
-                const int j = base + b * 32 + lane;
-                hv[b] = j < total ? wlist[j] : -1;
-                hd[b] = hv[b] >= 0 ? __ldg(p.head + hv[b]) : make_int2(-1, 0);
+        for (int b = 0; b < kPullVerts; ++b) {
+            const int j = base + b * 32 + lane;
+            v[b] = j < nmiss ? wlist[j] : -1;
+            par[b] = -1;
+            cur[b] = 0;
+            end[b] = 0;
+            deg[b] = 0;
+            if (v[b] >= 0) {
+                cur[b] = p.row_ptr[v[b]];
+                end[b] = p.row_ptr[v[b] + 1];
+                deg[b] = (int32_t)(end[b] - cur[b]);
             }
-#pragma unroll
-            for (int b = 0; b < kHeadVerts; ++b)
-                hf[b] = hd[b].x >= 0 ? ldcg(fcur + (hd[b].x >> 5)) : 0u;
-            __syncwarp();
-#pragma unroll
-            for (int b = 0; b < kHeadVerts; ++b) {
-                const bool hit = hd[b].x >= 0 && ((hf[b] >> (hd[b].x & 31)) & 1u);
-                if (hit)
-                    pull_resolve(p, k, t, wfound, w0, hv[b], hd[b].x, hd[b].y);
-                const bool miss = hv[b] >= 0 && !hit && hd[b].y > 1;
-                const unsigned mm = __ballot_sync(kFull, miss);
-                if (miss)
-                    wlist[nmiss + __popc(mm & ((1u << lane) - 1u))] = hv[b];
-                nmiss += __popc(mm);
-            }
-            __syncwarp();
         }
-        // Phase 2: the misses' rows in CSR order, two entries per round.
-        for (int base = 0; base < nmiss; base += 32 * kPullVerts) {
-            int32_t v[kPullVerts], par[kPullVerts], deg[kPullVerts];
-            RowT cur[kPullVerts], end[kPullVerts];
-#pragma unroll
-            for (int b = 0; b < kPullVerts; ++b) {
-                const int j = base + b * 32 + lane;
-                v[b] = j < nmiss ? wlist[j] : -1;
-                par[b] = -1;
-                cur[b] = 0;
-                end[b] = 0;
-                deg[b] = 0;
-                if (v[b] >= 0) {
-                    cur[b] = p.row_ptr[v[b]];
-                    end[b] = p.row_ptr[v[b] + 1];
-                    deg[b] = (int32_t)(end[b] - cur[b]);
-                }
-            }
-            for (int round = 0; round < kPullRounds; ++round) {
-                bool any = false;
-#pragma unroll
-                for (int b = 0; b < kPullVerts; ++b)
-                    any |= par[b] < 0 && cur[b] < end[b];
-                if (!__any_sync(kFull, any))
-                    break;
-                int32_t u0[kPullVerts], u1[kPullVerts];
-                uint32_t f0[kPullVerts], f1[kPullVerts];
-#pragma unroll
-                for (int b = 0; b < kPullVerts; ++b) {
-                    u0[b] = -1;
-                    u1[b] = -1;
-                    if (par[b] < 0 && cur[b] < end[b]) {
-                        u0[b] = p.col[cur[b]];
-                        if (cur[b] + 1 < end[b])
-                            u1[b] = p.col[cur[b] + 1];
-                    }
-                }
-#pragma unroll
-                for (int b = 0; b < kPullVerts; ++b) {
-                    f0[b] = u0[b] >= 0 ? ldcg(fcur + (u0[b] >> 5)) : 0u;
-                    f1[b] = u1[b] >= 0 ? ldcg(fcur + (u1[b] >> 5)) : 0u;
-                }
-                bool more = false;
-#pragma unroll
-                for (int b = 0; b < kPullVerts; ++b) {
-                    if (u0[b] >= 0) {
-                        if ((f0[b] >> (u0[b] & 31)) & 1u)
-                            par[b] = u0[b];
-                        else if (u1[b] >= 0 && ((f1[b] >> (u1[b] & 31)) & 1u))
-                            par[b] = u1[b];
-                        else
-                            cur[b] += 2;
-                    }
-                    more |= par[b] < 0 && cur[b] < end[b];
-                }
-                if (!__any_sync(kFull, more))
-                    break;
-            }
-            // Rows still open: the whole warp scans 32 entries per step.
-#pragma unroll
-            for (int b = 0; b < kPullVerts; ++b) {
-                unsigned mm = __ballot_sync(kFull, par[b] < 0 && cur[b] < end[b]);
-                while (mm) {
-                    const int src = __ffs(mm) - 1;
-                    mm &= mm - 1;
-                    const RowT cp = __shfl_sync(kFull, cur[b], src);
-                    const RowT ce = __shfl_sync(kFull, end[b], src);
-                    int32_t hitv = -1;
-                    for (RowT q = cp; q < ce && hitv < 0; q += 32) {
-                        const RowT e = q + lane;
-                        int32_t u = -1;
-                        bool hit = false;
-                        if (e < ce) {
-                            u = p.col[e];
-                            hit = (ldcg(fcur + (u >> 5)) >> (u & 31)) & 1u;
-                        }
-                        const unsigned hm = __ballot_sync(kFull, hit);
-                        if (hm)
-                            hitv = __shfl_sync(kFull, u, __ffs(hm) - 1);
-                    }
-                    if (lane == src) {
-                        par[b] = hitv;
-                        cur[b] = ce;
-                    }
-                }
-            }
+        for (int round = 0; round < kPullRounds; ++round) {
+            bool any = false;
 #pragma unroll
             for (int b = 0; b < kPullVerts; ++b)
-                if (par[b] >= 0)
-                    pull_resolve(p, k, t, wfound, w0, v[b], par[b], deg[b]);
+                any |= par[b] < 0 && cur[b] < end[b];
+            if (!__any_sync(kFull, any))
+                break;
+            int32_t u0[kPullVerts], u1[kPullVerts];
+            uint32_t f0[kPullVerts], f1[kPullVerts];
+#pragma unroll
+            for (int b = 0; b < kPullVerts; ++b) {
+                u0[b] = -1;
+                u1[b] = -1;
+                if (par[b] < 0 && cur[b] < end[b]) {
+                    u0[b] = p.col[cur[b]];
+                    if (cur[b] + 1 < end[b])
+                        u1[b] = p.col[cur[b] + 1];
+                }
+            }
+#pragma unroll
+            for (int b = 0; b < kPullVerts; ++b) {
+                f0[b] = u0[b] >= 0 ? ldcg(fcur + (u0[b] >> 5)) : 0u;
+                f1[b] = u1[b] >= 0 ? ldcg(fcur + (u1[b] >> 5)) : 0u;
+            }
+            bool more = false;
+#pragma unroll
+            for (int b = 0; b < kPullVerts; ++b) {
+                if (u0[b] >= 0) {
+                    if ((f0[b] >> (u0[b] & 31)) & 1u)
+                        par[b] = u0[b];
+                    else if (u1[b] >= 0 && ((f1[b] >> (u1[b] & 31)) & 1u))
+                        par[b] = u1[b];
+                    else
+                        cur[b] += 2;
+                }
+                more |= par[b] < 0 && cur[b] < end[b];
+            }
+            if (!__any_sync(kFull, more))
+                break;
+        }
+        // Rows still open: the whole warp scans 32 entries per step.
+#pragma unroll
+        for (int b = 0; b < kPullVerts; ++b) {
+            unsigned mm = __ballot_sync(kFull, par[b] < 0 && cur[b] < end[b]);
+            while (mm) {
+                const int src = __ffs(mm) - 1;
+                mm &= mm - 1;
+                const RowT cp = __shfl_sync(kFull, cur[b], src);
+                const RowT ce = __shfl_sync(kFull, end[b], src);
+                int32_t hitv = -1;
+                for (RowT q = cp; q < ce && hitv < 0; q += 32) {
+                    const RowT e = q + lane;
+                    int32_t u = -1;
+                    bool hit = false;
+                    if (e < ce) {
+                        u = p.col[e];
+                        hit = (ldcg(fcur + (u >> 5)) >> (u & 31)) & 1u;
+                    }
+                    const unsigned hm = __ballot_sync(kFull, hit);
+                    if (hm)
+                        hitv = __shfl_sync(kFull, u, __ffs(hm) - 1);
+                }
+                if (lane == src) {
+                    par[b] = hitv;
+                    cur[b] = ce;
+                }
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < kPullVerts; ++b)
+            if (par[b] >= 0)
+                pull_resolve(p, k, t, wfound, w0, v[b], par[b], deg[b]);
+    }
+}
+
+template <typename RowT>
+__device__ void pull_level(const Params<RowT>& p, int k, Tally& t, int32_t* wlist,
+                           uint32_t* wfound, uint32_t* wvis)
+{
+    uint32_t* fnext = p.fb[(k + 1) & 1];
+    const int lane = threadIdx.x & 31;
+    const long long gwarp = (long long)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    const long long nwarps = (long long)((gridDim.x * blockDim.x) >> 5);
+    const int wlo = (int)((long long)p.words * gwarp / nwarps);
+    const int whi = (int)((long long)p.words * (gwarp + 1) / nwarps);
+    for (int a = wlo; a < whi; a += kPullWin) {
+        const int nwin = min(kPullWin, whi - a);
+        // Stage the window's visited words (padding words read as visited).
+#pragma unroll
+        for (int j = 0; j < kPullWin / 32; ++j) {
+            const int i = 32 * j + lane;
+            wvis[i] = i < nwin ? ldcg(p.visited + a + i) : kFull;
+            wfound[i] = 0u;
         }
         __syncwarp();
-        if (lane < cw && w < p.words) {
-            const uint32_t f = wfound[lane];
-            if (f != 0u)
-                __stcg(p.visited + w, vis | f);
-            __stcg(fnext + w, f);
+        // Compact 32 words at a time; a step whose vertices would overflow
+        // the list runs the pass on the list first. One call site.
+        int j = 0, nl = 0;
+        for (;;) {
+            bool run = j >= kPullWin / 32;
+            if (!run) {
+                const uint32_t todo = ~wvis[32 * j + lane];
+                const int cnt = __popc(todo);
+                const int incl = warp_inclusive_scan(cnt);
+                const int tot = __shfl_sync(kFull, incl, 31);
+                if (nl + tot <= kPullList) {
+                    int pos = nl + incl - cnt;
+                    uint32_t m = todo;
+                    const int w = a + 32 * j + lane;
+                    while (m) {
+                        const int bit = __ffs(m) - 1;
+                        m &= m - 1;
+                        wlist[pos++] = (w << 5) + bit;
+                    }
+                    nl += tot;
+                    ++j;
+                    continue;
+                }
+                run = true;
+            }
+            __syncwarp();
+            if (nl > 0)
+                pull_list(p, k, t, wlist, nl, wfound, a);
+            __syncwarp();
+            nl = 0;
+            if (j >= kPullWin / 32)
+                break;
+        }
+#pragma unroll
+        for (int jj = 0; jj < kPullWin / 32; ++jj) {
+            const int i = 32 * jj + lane;
+            if (i < nwin) {
+                const uint32_t f = wfound[i];
+                if (f != 0u)
+                    __stcg(p.visited + a + i, wvis[i] | f);
+                __stcg(fnext + a + i, f);
+            }
         }
         __syncwarp();
-      }
     }
 }
 
@@ -1322,6 +1381,55 @@ __device__ void solo_levels(const Params<RowT>& p, int k, int qn, RowT qm, long 
     }
 }
 
+// ------------------------------------------------------------ S10 output
+
+// dist from the hop codes, once the search has ended. A warp converts 1,024
+// consecutive vertices per step: lane l reads the 4 codes of vertices
+// base + 128 q + 4 l (q = 0..7) as one word each and writes their distances
+// as one 16-byte store each, so every store instruction of the warp covers
+// 512 contiguous bytes and all eight code loads are in flight together.
+// Codes of kHopFar keep the distance their discovery wrote to dist.
+__device__ __forceinline__ int32_t hop_to_dist(uint32_t c, const int32_t* dist, int64_t v)
+{
+    return c == 0u ? -1 : (c == kHopFar ? ldcg(dist + v) : (int32_t)c - 1);
+}
+
+template <typename RowT>
+__device__ void write_dist(const Params<RowT>& p)
+{
+    constexpr int kQ = 8;
+    const int64_t n = p.n;
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const uint32_t* h4 = reinterpret_cast<const uint32_t*>(p.hop);  // 16-byte aligned
+    const bool vec = (reinterpret_cast<uintptr_t>(p.dist) & 15u) == 0;
+    const int64_t nfull = vec ? n / (128 * kQ) : 0;   // steps with every vertex < n
+    for (int64_t st = gw; st < nfull; st += nw) {
+        const int64_t base = st * 128 * kQ;
+        uint32_t c[kQ];
+#pragma unroll
+        for (int q = 0; q < kQ; ++q)
+            c[q] = ldcg(h4 + ((base + 128 * q) >> 2) + lane);
+#pragma unroll
+        for (int q = 0; q < kQ; ++q) {
+            const int64_t v = base + 128 * q + 4 * lane;
+            int4 o;
+            o.x = hop_to_dist(c[q] & 0xffu, p.dist, v);
+            o.y = hop_to_dist((c[q] >> 8) & 0xffu, p.dist, v + 1);
+            o.z = hop_to_dist((c[q] >> 16) & 0xffu, p.dist, v + 2);
+            o.w = hop_to_dist(c[q] >> 24, p.dist, v + 3);
+            *reinterpret_cast<int4*>(p.dist + v) = o;
+        }
+    }
+    // The rest (or everything when dist is not 16-byte aligned), one vertex
+    // per thread.
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t v = nfull * 128 * kQ + tid; v < n; v += stride)
+        p.dist[v] = hop_to_dist(ldcg(p.hop + v), p.dist, v);
+}
+
 // ------------------------------------------------------------ kernels
 
 // Dynamic shared memory: the compaction stage (row starts, degrees, vertices)
@@ -1355,7 +1463,7 @@ __host__ __device__ inline size_t level_smem_bytes(int bd)
 {
     const size_t tile = (size_t)bd * kItems;
     const size_t push = (sizeof(RowT) + 8) * tile + (2 * sizeof(RowT) + 4) * (tile + 1) + 16;
-    const size_t pull = (size_t)(bd / 32) * (1024 + 32) * sizeof(uint32_t);
+    const size_t pull = (size_t)(bd / 32) * (kPullList + 2 * kPullWin) * sizeof(uint32_t);
     const size_t wstage = (size_t)(bd / 32) * kWarpStage * (sizeof(RowT) + 8);
     const size_t m = push > pull ? push : pull;
     return m > wstage ? m : wstage;
@@ -1377,6 +1485,7 @@ __global__ void __launch_bounds__(512, 2) level_kernel(Params<RowT> p)
     int budget = p.level_budget;
     const long long nonisolated = ldcg(&p.ctl->nonisolated);
     const bool leader = blockIdx.x == 0 && threadIdx.x == 0;
+    bool finished = false;      // this launch saw the search end
     __syncthreads();
 
     for (;;) {
@@ -1392,8 +1501,12 @@ __global__ void __launch_bounds__(512, 2) level_kernel(Params<RowT> p)
         const int prev_dir = ldcg(&prv->dir);
         const int done = ldcg(&p.ctl->done);
         const int status = ldcg(&p.ctl->status);
-        if (done != 0 || status != BFS_CSR_OK)
+        if (done != 0 || status != BFS_CSR_OK) {
+            // done may also come from CTA 0 ending the search in this very
+            // iteration; the hop codes are final either way.
+            finished = done != 0 && status == BFS_CSR_OK;
             break;
+        }
         const long long F = (long long)found;
         if (F == 0 || (p.max_depth >= 0 && k >= p.max_depth)) {
             if (leader) {
@@ -1420,6 +1533,7 @@ __global__ void __launch_bounds__(512, 2) level_kernel(Params<RowT> p)
                 __threadfence();
                 p.ctl->done = 1;
             }
+            finished = true;
             break;
         }
         if (budget <= 0)
@@ -1468,10 +1582,10 @@ __global__ void __launch_bounds__(512, 2) level_kernel(Params<RowT> p)
             }
             {
                 const int wid = threadIdx.x >> 5;
-                int32_t* wlist = reinterpret_cast<int32_t*>(smem_raw) + wid * 1024;
+                int32_t* wlist = reinterpret_cast<int32_t*>(smem_raw) + wid * kPullList;
                 uint32_t* wfound = reinterpret_cast<uint32_t*>(smem_raw) +
-                                   (blockDim.x >> 5) * 1024 + wid * 32;
-                pull_level(p, k, t, wlist, wfound);
+                                   (blockDim.x >> 5) * kPullList + wid * 2 * kPullWin;
+                pull_level(p, k, t, wlist, wfound, wfound + kPullWin);
             }
         } else {
             if (prev_dir == BFS_CSR_DIR_PULL) {
@@ -1525,6 +1639,11 @@ __global__ void __launch_bounds__(512, 2) level_kernel(Params<RowT> p)
         --budget;
     }
 
+    // S10: every CTA saw the same empty (or depth-bounded) frontier after
+    // the last grid barrier, so all hop codes are final.
+    if (finished && p.defer_dist)
+        write_dist(p);
+
     // Leave: the last CTA out resets the barrier for the next launch.
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -1540,10 +1659,12 @@ __global__ void __launch_bounds__(512, 2) level_kernel(Params<RowT> p)
     }
 }
 
-// S1: reset the run state and seed the source. dist and parent are filled
-// with -1 (source: 0 and itself), visited starts as the dead bitmap (vertices
-// of degree 0 and padding bits beyond n) plus the source bit, and slot 0
-// holds F_0 = {source}.
+// S1: reset the run state and seed the source. parent is filled with -1
+// (source: itself); with bitmap discovery the hop codes are cleared (source:
+// distance 0) and dist is left to the end of the search, otherwise dist is
+// filled with -1 (source: 0). visited starts as the dead bitmap (vertices of
+// degree 0 and padding bits beyond n) plus the source bit, and slot 0 holds
+// F_0 = {source}.
 template <typename RowT>
 __global__ void init_kernel(Params<RowT> p, const uint32_t* __restrict__ dead, int32_t source,
                             int use_dead)
@@ -1551,33 +1672,38 @@ __global__ void init_kernel(Params<RowT> p, const uint32_t* __restrict__ dead, i
     const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     const int32_t n = p.n;
-    const int64_t n4 = n / 4;
-    int4* d4 = reinterpret_cast<int4*>(p.dist);
-    int4* p4 = reinterpret_cast<int4*>(p.parent);
-    const int4 neg = make_int4(-1, -1, -1, -1);
-    const bool aligned = (reinterpret_cast<uintptr_t>(p.dist) & 15u) == 0 &&
-                         (p.parent == nullptr || (reinterpret_cast<uintptr_t>(p.parent) & 15u) == 0);
-    if (aligned) {
-        for (int64_t i = tid; i < n4; i += stride) {
-            int4 dv = neg, pv = neg;
-            if (source / 4 == i) {
-                (&dv.x)[source & 3] = 0;
-                (&pv.x)[source & 3] = source;
+    const bool wdist = !p.defer_dist;
+    int32_t* outs[2] = {wdist ? p.dist : nullptr, p.parent};
+    const int32_t seed[2] = {0, source};
+    for (int o = 0; o < 2; ++o) {
+        int32_t* a = outs[o];
+        if (a == nullptr)
+            continue;
+        if ((reinterpret_cast<uintptr_t>(a) & 15u) == 0) {
+            const int64_t n4 = n / 4;
+            int4* a4 = reinterpret_cast<int4*>(a);
+            for (int64_t i = tid; i < n4; i += stride) {
+                int4 x = make_int4(-1, -1, -1, -1);
+                if (source / 4 == i)
+                    (&x.x)[source & 3] = seed[o];
+                a4[i] = x;
             }
-            d4[i] = dv;
-            if (p.parent != nullptr)
-                p4[i] = pv;
+            for (int64_t i = n4 * 4 + tid; i < n; i += stride)
+                a[i] = i == source ? seed[o] : -1;
+        } else {
+            for (int64_t i = tid; i < n; i += stride)
+                a[i] = i == source ? seed[o] : -1;
         }
-        for (int64_t i = n4 * 4 + tid; i < n; i += stride) {
-            p.dist[i] = i == source ? 0 : -1;
-            if (p.parent != nullptr)
-                p.parent[i] = i == source ? source : -1;
-        }
-    } else {
-        for (int64_t i = tid; i < n; i += stride) {
-            p.dist[i] = i == source ? 0 : -1;
-            if (p.parent != nullptr)
-                p.parent[i] = i == source ? source : -1;
+    }
+    if (p.defer_dist) {
+        // The hop region is 16-byte aligned and padded to a multiple of 16.
+        uint4* h16 = reinterpret_cast<uint4*>(p.hop);
+        const int64_t n16 = ((int64_t)n + 15) / 16;
+        for (int64_t i = tid; i < n16; i += stride) {
+            uint4 z = make_uint4(0u, 0u, 0u, 0u);
+            if (source / 16 == i)
+                (&z.x)[(source & 15) >> 2] = 1u << (8 * (source & 3));
+            h16[i] = z;
         }
     }
     for (int64_t w = tid; w < p.words; w += stride) {
