@@ -44,7 +44,7 @@ EXPORTED = [
     "bfs_csr_run_init", "bfs_csr_run_levels",
     "bfs_csr_sync", "bfs_csr_level_stats", "bfs_csr_create_host", "bfs_csr_run_host",
     "bfs_csr_run_host_batch", "bfs_csr_destroy", "bfs_csr_status_string", "bfs_csr_last_cuda_error",
-    "bfs_csr_run_noalloc",
+    "bfs_csr_run_noalloc", "bfs_csr_run_batch",
 ]
 BFS_CSR_NOALLOC_MAX_VERTICES = 1048576
 
@@ -68,7 +68,8 @@ class bfs_csr_options(ctypes.Structure):
         ("test_unreachable_barrier", ctypes.c_int32),
         ("push_beta", ctypes.c_int32),
         ("narrow_max_edges", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 5),
+        ("lanes", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 4),
     ]
 
 
@@ -108,6 +109,7 @@ _sig = {
     "bfs_csr_last_cuda_error": ([_vp], _i32),
     "bfs_csr_run_noalloc": ([_i64, _i64, _vp, _vp, _i32, _i64, _vp, _vp, _vp,
                              ctypes.POINTER(ctypes.c_int32), _opt_p, _vp], _i32),
+    "bfs_csr_run_batch": ([_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp], _i32),
 }
 for _name, (_args, _res) in _sig.items():
     _f = getattr(_lib, _name)
@@ -215,6 +217,27 @@ class BfsCsr:
         _check(bfs_csr_sync(self.handle, _stream_ptr(stream), ctypes.byref(levels)),
                "bfs_csr_sync", self.handle)
         return int(levels.value)
+
+    def run_batch(self, sources, dist, parent=None, num_levels=None, stamps=None,
+                  stream=None) -> None:
+        """Search from every source (waits): row i of dist / parent (int32 CUDA
+        tensors of len(sources) x n) gets source i's result, num_levels[i]
+        (int32 CUDA tensor) its level count. The searches run on the handle's
+        options.lanes lanes at once. stamps: int64 CUDA tensor of
+        3 x len(sources) for the device timer (ns) at each search's init,
+        level-loop start and level-loop end, or None."""
+        import numpy as np
+        src = np.ascontiguousarray(np.asarray(sources, dtype=np.int64))
+        k = int(src.shape[0])
+        for a in (dist, parent):
+            if a is not None and (a.numel() != k * self.n or not a.is_contiguous()):
+                raise ValueError("dist/parent must be contiguous len(sources) x n tensors")
+        status = bfs_csr_run_batch(self.handle, k, src.ctypes.data, dist.data_ptr(),
+                                   parent.data_ptr() if parent is not None else None,
+                                   num_levels.data_ptr() if num_levels is not None else None,
+                                   stamps.data_ptr() if stamps is not None else None,
+                                   _stream_ptr(stream))
+        _check(status, "bfs_csr_run_batch", self.handle)
 
     def search(self, source: int, want_parent: bool = True, stream=None):
         """Run one search and wait: returns (dist, parent or None, num_levels)."""

@@ -26,13 +26,20 @@ namespace {
 constexpr int kStatsCap = 1 << 16;
 constexpr int kDefaultBlock = 512;
 
+constexpr int kMaxLanes = 8;
+
+// Workspace: the graph part (dead bitmap, head array), derived once per CSR,
+// then one search part per lane; the offsets below are lane 0's, lane j's
+// are `search` bytes further on.
 struct Layout {
-    size_t ctl, visited, dead, head, hop, fb0, fb1, qv0, qv1, qbeg0, qbeg1, qoff0, qoff1, stats, total;
+    size_t dead, head;
+    size_t ctl, visited, hop, fb0, fb1, qv0, qv1, qbeg0, qbeg1, qoff0, qoff1, stats;
+    size_t search, total;
 };
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-Layout make_layout(int64_t n, int row_ptr_64)
+Layout make_layout(int64_t n, int row_ptr_64, int lanes = 1)
 {
     Layout L;
     const size_t words = (size_t)((n + 31) / 32);
@@ -43,10 +50,11 @@ Layout make_layout(int64_t n, int row_ptr_64)
         off = align_up(off + bytes, 256);
         return at;
     };
-    L.ctl = take(sizeof(Ctl));
-    L.visited = take(words * 4);
     L.dead = take(words * 4);
     L.head = take((size_t)n * 8);
+    const size_t search0 = off;
+    L.ctl = take(sizeof(Ctl));
+    L.visited = take(words * 4);
     L.hop = take(align_up((size_t)n, 16));
     L.fb0 = take(words * 4);
     L.fb1 = take(words * 4);
@@ -57,7 +65,8 @@ Layout make_layout(int64_t n, int row_ptr_64)
     L.qoff0 = take((size_t)n * R);
     L.qoff1 = take((size_t)n * R);
     L.stats = take((size_t)kStatsCap * sizeof(bfs_csr_level_stat));
-    L.total = off;
+    L.search = off - search0;
+    L.total = off + (size_t)(lanes - 1) * L.search;
     return L;
 }
 
@@ -104,6 +113,12 @@ struct bfs_csr_t {
     cudaStream_t copy_stream = nullptr;
     cudaEvent_t ev_search[2] = {nullptr, nullptr};
     cudaEvent_t ev_copy[2] = {nullptr, nullptr};
+    // device batches: one stream per lane and the fork/join events (made on
+    // first use)
+    int lanes = 1;
+    cudaStream_t lane_stream[kMaxLanes] = {};
+    cudaEvent_t ev_fork = nullptr;
+    cudaEvent_t ev_join[kMaxLanes] = {};
 };
 
 namespace {
@@ -136,6 +151,8 @@ int check_options(const bfs_csr_options& o)
     if (o.block_threads != 0 && (o.block_threads < 64 || o.block_threads > 512 || o.block_threads % 32))
         return BFS_CSR_EINVAL;
     if (o.grid_blocks < 0 || o.barrier_timeout_ns <= 0 || o.narrow_max_edges < 0)
+        return BFS_CSR_EINVAL;
+    if (o.lanes < 0 || o.lanes > kMaxLanes)
         return BFS_CSR_EINVAL;
     return BFS_CSR_OK;
 }
@@ -175,11 +192,13 @@ int configure_grid(bfs_csr_t* h)
 }
 
 template <typename RowT>
-Params<RowT> make_params(bfs_csr_t* h, int32_t* d_dist, int32_t* d_parent, int32_t* d_levels)
+Params<RowT> make_params(bfs_csr_t* h, int32_t* d_dist, int32_t* d_parent, int32_t* d_levels,
+                         int lane = 0)
 {
     Params<RowT> p;
     std::memset(&p, 0, sizeof(p));
-    unsigned char* w = h->ws;
+    unsigned char* g = h->ws;                                // graph part
+    unsigned char* w = h->ws + (size_t)lane * h->L.search;   // this lane's search part
     p.row_ptr = static_cast<const RowT*>(h->row_ptr);
     p.col = h->col;
     p.n = (int32_t)h->n;
@@ -187,8 +206,8 @@ Params<RowT> make_params(bfs_csr_t* h, int32_t* d_dist, int32_t* d_parent, int32
     p.dist = d_dist;
     p.parent = d_parent;
     p.visited = reinterpret_cast<uint32_t*>(w + h->L.visited);
-    p.dead = reinterpret_cast<const uint32_t*>(w + h->L.dead);
-    p.head = reinterpret_cast<const int2*>(w + h->L.head);
+    p.dead = reinterpret_cast<const uint32_t*>(g + h->L.dead);
+    p.head = reinterpret_cast<const int2*>(g + h->L.head);
     p.hop = reinterpret_cast<uint8_t*>(w + h->L.hop);
     p.defer_dist = h->opt.discovery == BFS_CSR_DISC_BITMAP ? 1 : 0;
     p.vec_out = ((reinterpret_cast<uintptr_t>(d_dist) & 15u) == 0 &&
@@ -235,7 +254,8 @@ int prepare(bfs_csr_t* h, cudaStream_t s)
 {
     unsigned char* w = h->ws;
     Ctl* ctl = reinterpret_cast<Ctl*>(w + h->L.ctl);
-    FBC_CUDA(h, cudaMemsetAsync(ctl, 0, sizeof(Ctl), s));
+    for (int j = 0; j < h->lanes; ++j)
+        FBC_CUDA(h, cudaMemsetAsync(w + (size_t)j * h->L.search + h->L.ctl, 0, sizeof(Ctl), s));
     const RowT* rp = static_cast<const RowT*>(h->row_ptr);
     if (h->opt.validate) {
         fbc::validate_kernel<RowT><<<init_grid(h), 256, 0, s>>>(rp, h->col, h->n, h->nnz,
@@ -251,6 +271,12 @@ int prepare(bfs_csr_t* h, cudaStream_t s)
     fbc::dead_kernel<RowT><<<init_grid(h), 256, 0, s>>>(
         rp, (int32_t)h->n, h->words, reinterpret_cast<uint32_t*>(w + h->L.dead), &ctl->nonisolated);
     FBC_CUDA(h, cudaGetLastError());
+    // Every lane's control block carries the non-isolated count.
+    for (int j = 1; j < h->lanes; ++j) {
+        Ctl* cj = reinterpret_cast<Ctl*>(w + (size_t)j * h->L.search + h->L.ctl);
+        FBC_CUDA(h, cudaMemcpyAsync(&cj->nonisolated, &ctl->nonisolated, sizeof(long long),
+                                    cudaMemcpyDeviceToDevice, s));
+    }
     fbc::head_kernel<RowT><<<init_grid(h), 256, 0, s>>>(rp, h->col, (int32_t)h->n,
                                                          reinterpret_cast<int2*>(w + h->L.head));
     FBC_CUDA(h, cudaGetLastError());
@@ -259,9 +285,11 @@ int prepare(bfs_csr_t* h, cudaStream_t s)
 }
 
 template <typename RowT>
-int launch_init(bfs_csr_t* h, int32_t source, int32_t* d_dist, int32_t* d_parent, cudaStream_t s)
+int launch_init(bfs_csr_t* h, int32_t source, int32_t* d_dist, int32_t* d_parent, cudaStream_t s,
+                int lane = 0, long long* stamps = nullptr)
 {
-    Params<RowT> p = make_params<RowT>(h, d_dist, d_parent, nullptr);
+    Params<RowT> p = make_params<RowT>(h, d_dist, d_parent, nullptr, lane);
+    p.stamps = stamps;
     const uint32_t* dead = reinterpret_cast<const uint32_t*>(h->ws + h->L.dead);
     fbc::init_kernel<RowT><<<init_grid(h), 256, 0, s>>>(p, dead, source, h->symmetric ? 1 : 0);
     FBC_CUDA(h, cudaGetLastError());
@@ -270,20 +298,23 @@ int launch_init(bfs_csr_t* h, int32_t source, int32_t* d_dist, int32_t* d_parent
 
 template <typename RowT>
 int launch_levels(bfs_csr_t* h, int32_t* d_dist, int32_t* d_parent, int32_t* d_levels,
-                  cudaStream_t s)
+                  cudaStream_t s, int lane = 0, int grid = 0, long long* stamps = nullptr)
 {
-    Params<RowT> p = make_params<RowT>(h, d_dist, d_parent, d_levels);
+    Params<RowT> p = make_params<RowT>(h, d_dist, d_parent, d_levels, lane);
+    p.stamps = stamps;
     void* args[] = {&p};
+    if (grid <= 0)
+        grid = h->grid;
     if (h->opt.loop_mode == BFS_CSR_LOOP_PERSISTENT) {
-        FBC_CUDA(h, cudaLaunchCooperativeKernel(level_kernel_ptr<RowT>(), dim3(h->grid),
+        FBC_CUDA(h, cudaLaunchCooperativeKernel(level_kernel_ptr<RowT>(), dim3(grid),
                                                 dim3(h->block), args, h->smem, s));
         return BFS_CSR_OK;
     }
     // Host loop: one launch per level and a device->host read of the state.
-    Ctl* ctl = reinterpret_cast<Ctl*>(h->ws + h->L.ctl);
+    Ctl* ctl = reinterpret_cast<Ctl*>(h->ws + (size_t)lane * h->L.search + h->L.ctl);
     p.level_budget = 1;
     for (;;) {
-        FBC_CUDA(h, cudaLaunchCooperativeKernel(level_kernel_ptr<RowT>(), dim3(h->grid),
+        FBC_CUDA(h, cudaLaunchCooperativeKernel(level_kernel_ptr<RowT>(), dim3(grid),
                                                 dim3(h->block), args, h->smem, s));
         int state[2] = {0, 0};  // status, done
         FBC_CUDA(h, cudaMemcpyAsync(state, &ctl->status, sizeof(state), cudaMemcpyDeviceToHost, s));
@@ -296,7 +327,8 @@ int launch_levels(bfs_csr_t* h, int32_t* d_dist, int32_t* d_parent, int32_t* d_l
 
 int create_common(bfs_csr_t* h, void* d_workspace, size_t workspace_bytes, cudaStream_t s)
 {
-    h->L = make_layout(h->n, h->row_ptr_64);
+    h->lanes = h->opt.lanes > 1 ? h->opt.lanes : 1;
+    h->L = make_layout(h->n, h->row_ptr_64, h->lanes);
     h->words = (int)((h->n + 31) / 32);
     if (d_workspace != nullptr) {
         if (workspace_bytes < h->L.total || (reinterpret_cast<uintptr_t>(d_workspace) & 255u))
@@ -346,6 +378,11 @@ void release(bfs_csr_t* h)
         if (h->ev_copy[i]) cudaEventDestroy(h->ev_copy[i]);
     }
     if (h->copy_stream) cudaStreamDestroy(h->copy_stream);
+    for (int j = 0; j < kMaxLanes; ++j) {
+        if (h->lane_stream[j]) cudaStreamDestroy(h->lane_stream[j]);
+        if (h->ev_join[j]) cudaEventDestroy(h->ev_join[j]);
+    }
+    if (h->ev_fork) cudaEventDestroy(h->ev_fork);
     delete h;
 }
 
@@ -410,6 +447,7 @@ int bfs_csr_default_options(bfs_csr_options* o)
     o->barrier_timeout_ns = 10ll * 1000 * 1000 * 1000;
     o->test_unreachable_barrier = 0;
     o->narrow_max_edges = 2048;
+    o->lanes = 1;
     return BFS_CSR_OK;
 }
 
@@ -421,7 +459,8 @@ int bfs_csr_workspace_bytes(int64_t n, int64_t nnz, int row_ptr_64, const bfs_cs
     const int rc = validate_shape(n, nnz, row_ptr_64, opt);
     if (rc != BFS_CSR_OK)
         return rc;
-    *bytes = make_layout(n, row_ptr_64).total;
+    const int lanes = opt != nullptr && opt->lanes > 1 ? opt->lanes : 1;
+    *bytes = make_layout(n, row_ptr_64, lanes).total;
     return BFS_CSR_OK;
 }
 
@@ -699,6 +738,102 @@ int bfs_csr_run_host_batch(bfs_csr_handle h, int32_t num_sources, const int64_t*
     }
     h->last_status = st[4 * (num_sources - 1)];
     h->last_num_levels = st[4 * (num_sources - 1) + 3];
+    return first_bad;
+}
+
+int bfs_csr_run_batch(bfs_csr_handle h, int32_t num_sources, const int64_t* sources,
+                      int32_t* d_dist, int32_t* d_parent, int32_t* d_num_levels,
+                      int64_t* d_stamps, void* stream)
+{
+    if (h == nullptr || num_sources <= 0 || sources == nullptr || d_dist == nullptr)
+        return BFS_CSR_EINVAL;
+    for (int32_t i = 0; i < num_sources; ++i)
+        if (sources[i] < 0 || sources[i] >= h->n)
+            return BFS_CSR_EINVAL;
+    if (h->opt.direction == BFS_CSR_DIR_PULL && !h->symmetric)
+        return BFS_CSR_EUNSUPPORTED;
+    cudaStream_t s = as_stream(stream);
+    const bool concurrent = h->lanes > 1 && h->opt.loop_mode == BFS_CSR_LOOP_PERSISTENT;
+    const int lanes = concurrent ? h->lanes : 1;
+    if (concurrent && h->ev_fork == nullptr) {
+        FBC_CUDA(h, cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming));
+        for (int j = 0; j < h->lanes; ++j) {
+            FBC_CUDA(h, cudaStreamCreateWithFlags(&h->lane_stream[j], cudaStreamNonBlocking));
+            FBC_CUDA(h, cudaEventCreateWithFlags(&h->ev_join[j], cudaEventDisableTiming));
+        }
+    }
+    if (num_sources > h->batch_cap) {
+        if (h->d_batch != nullptr) {
+            FBC_CUDA(h, cudaFree(h->d_batch));
+            h->d_batch = nullptr;
+            h->batch_cap = 0;
+        }
+        FBC_CUDA(h, cudaMalloc(&h->d_batch, (size_t)num_sources * 4 * sizeof(int32_t)));
+        h->batch_cap = num_sources;
+    }
+    // Each lane's level kernel gets an equal share of the cooperative grid.
+    const int grid = concurrent ? (h->grid / lanes > 0 ? h->grid / lanes : 1) : h->grid;
+    if (concurrent) {
+        FBC_CUDA(h, cudaEventRecord(h->ev_fork, s));
+        for (int j = 0; j < lanes; ++j)
+            FBC_CUDA(h, cudaStreamWaitEvent(h->lane_stream[j], h->ev_fork, 0));
+    }
+    int rc = BFS_CSR_OK;
+    for (int32_t i = 0; i < num_sources && rc == BFS_CSR_OK; ++i) {
+        const int j = i % lanes;
+        cudaStream_t ls = concurrent ? h->lane_stream[j] : s;
+        const size_t row = (size_t)i * (size_t)h->n;
+        int32_t* dd = d_dist + row;
+        int32_t* dp = d_parent != nullptr ? d_parent + row : nullptr;
+        int32_t* dl = d_num_levels != nullptr ? d_num_levels + i : nullptr;
+        long long* st = d_stamps != nullptr ? reinterpret_cast<long long*>(d_stamps) + 3 * i
+                                            : nullptr;
+        rc = h->row_ptr_64 ? launch_init<int64_t>(h, (int32_t)sources[i], dd, dp, ls, j, st)
+                           : launch_init<int32_t>(h, (int32_t)sources[i], dd, dp, ls, j, st);
+        if (rc == BFS_CSR_OK)
+            rc = h->row_ptr_64 ? launch_levels<int64_t>(h, dd, dp, dl, ls, j, grid, st)
+                               : launch_levels<int32_t>(h, dd, dp, dl, ls, j, grid, st);
+        if (rc == BFS_CSR_OK) {
+            // The search's end state (status, done, level, level count).
+            const Ctl* cj = reinterpret_cast<const Ctl*>(h->ws + (size_t)j * h->L.search + h->L.ctl);
+            const cudaError_t e = cudaMemcpyAsync(h->d_batch + 4 * i, &cj->status,
+                                                  4 * sizeof(int32_t), cudaMemcpyDeviceToDevice, ls);
+            if (e != cudaSuccess)
+                rc = cuda_fail(h, e);
+        }
+    }
+    if (concurrent) {
+        for (int j = 0; j < lanes; ++j) {
+            cudaError_t e = cudaEventRecord(h->ev_join[j], h->lane_stream[j]);
+            if (e == cudaSuccess)
+                e = cudaStreamWaitEvent(s, h->ev_join[j], 0);
+            if (e != cudaSuccess && rc == BFS_CSR_OK)
+                rc = cuda_fail(h, e);
+        }
+    }
+    std::vector<int32_t> st((size_t)num_sources * 4, 0);
+    if (rc == BFS_CSR_OK) {
+        cudaError_t e = cudaMemcpyAsync(st.data(), h->d_batch, st.size() * sizeof(int32_t),
+                                        cudaMemcpyDeviceToHost, s);
+        if (e != cudaSuccess)
+            rc = cuda_fail(h, e);
+    }
+    const cudaError_t se = cudaStreamSynchronize(s);
+    if (se != cudaSuccess && rc == BFS_CSR_OK)
+        rc = cuda_fail(h, se);
+    h->last_num_levels = 0;   // batch searches keep no level records
+    if (rc != BFS_CSR_OK) {
+        h->last_status = rc;
+        return rc;
+    }
+    int first_bad = BFS_CSR_OK;
+    for (int32_t i = 0; i < num_sources; ++i) {
+        const int status = st[4 * i], done = st[4 * i + 1];
+        const int r = status != BFS_CSR_OK ? status : (done == 0 ? BFS_CSR_EDEVICE : BFS_CSR_OK);
+        if (r != BFS_CSR_OK && first_bad == BFS_CSR_OK)
+            first_bad = r;
+    }
+    h->last_status = first_bad;
     return first_bad;
 }
 

@@ -123,6 +123,7 @@ struct Params {
     long long timeout_ns;
     int unreachable_barrier;
     int narrow_max;             // single-CTA levels: frontier edges (and vertices) <= this
+    long long* stamps;          // may be null: global timer at init, level-loop start and end
 };
 
 // ------------------------------------------------------------ primitives
@@ -1483,6 +1484,8 @@ __global__ void __launch_bounds__(512, 2) level_kernel(Params<RowT> p)
     unsigned long long target = 0;
     int k = ldcg(&p.ctl->level);
     int budget = p.level_budget;
+    if (p.stamps != nullptr && k == 0 && blockIdx.x == 0 && threadIdx.x == 0)
+        p.stamps[1] = (long long)global_timer_ns();
     const long long nonisolated = ldcg(&p.ctl->nonisolated);
     const bool leader = blockIdx.x == 0 && threadIdx.x == 0;
     bool finished = false;      // this launch saw the search end
@@ -1652,6 +1655,8 @@ __global__ void __launch_bounds__(512, 2) level_kernel(Params<RowT> p)
         __threadfence();
         const unsigned int prev = atomicAdd(&p.ctl->exit_count, 1u);
         if (prev == gridDim.x - 1) {
+            if (p.stamps != nullptr && finished)
+                p.stamps[2] = (long long)global_timer_ns();
             p.ctl->bar = 0ull;
             p.ctl->exit_count = 0u;
             __threadfence();
@@ -1673,6 +1678,8 @@ __global__ void init_kernel(Params<RowT> p, const uint32_t* __restrict__ dead, i
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     const int32_t n = p.n;
     const bool wdist = !p.defer_dist;
+    if (p.stamps != nullptr && tid == 0)
+        p.stamps[0] = (long long)global_timer_ns();
     int32_t* outs[2] = {wdist ? p.dist : nullptr, p.parent};
     const int32_t seed[2] = {0, source};
     for (int o = 0; o < 2; ++o) {

@@ -87,7 +87,11 @@ typedef struct bfs_csr_options {
                                         edges (and vertices) run on one CTA without
                                         grid barriers; 0 disables; capped at the CTA's
                                         stage (block_threads * 4); default 2048 */
-    int32_t reserved[5];             /* zero */
+    int32_t lanes;                   /* searches bfs_csr_run_batch keeps in flight at once,
+                                        1..8 (0 means 1); each has its own search state
+                                        in the workspace and 1/lanes of the level
+                                        kernel's CTAs; default 1 */
+    int32_t reserved[4];             /* zero */
 } bfs_csr_options;
 
 /* Per-level record, kept when the run completes (see bfs_csr_level_stats). */
@@ -153,7 +157,9 @@ int bfs_csr_run(bfs_csr_handle h, int64_t source, int32_t *d_dist,
 /*
  * The two halves of bfs_csr_run, for callers that time or schedule them
  * separately: bfs_csr_run_init resets the run state and seeds `source`
- * (dist/parent filled with -1, source with 0 / itself: one kernel);
+ * (one kernel: parent filled with -1 and the source's set to itself, the
+ * per-search state cleared; dist is written by the level loop when the
+ * search ends, or, with BFS_CSR_DISC_CAS, filled with -1 here);
  * bfs_csr_run_levels then runs the level loop (one cooperative kernel, or
  * one launch per level in the host loop mode) on the outputs given to the
  * preceding bfs_csr_run_init of this handle. Same arguments, errors and
@@ -167,6 +173,29 @@ int bfs_csr_run_levels(bfs_csr_handle h, int32_t *d_num_levels, void *stream);
 /* Wait for the handle's last run on `stream`; return its device status and
  * store the level count in *num_levels (may be NULL). */
 int bfs_csr_sync(bfs_csr_handle h, void *stream, int32_t *num_levels);
+
+/*
+ * Search from each of num_sources sources (host array) and wait. Source i's
+ * dist and parent go to row i of d_dist and d_parent (device, num_sources x n
+ * int32, row-major; d_parent may be NULL) and its level count to
+ * d_num_levels[i] (device, may be NULL). The searches run on the handle's
+ * opt.lanes lanes: lane j takes sources j, j + lanes, ... in order, on a
+ * stream of its own forked from and joined back to `stream`, with its own
+ * search state and 1/lanes of the level kernel's CTAs, so searches on
+ * different lanes overlap: while one runs its narrow, latency-bound levels or
+ * grid barriers, another keeps the memory system busy. Not a construct of the
+ * pages, whose searches run one at a time; an independent search per source,
+ * each with the result a single bfs_csr_run would give. d_stamps (device,
+ * 3 x num_sources int64, may be NULL) receives, per search, the device
+ * global timer (ns) when its init kernel, its level loop and the end of its
+ * level loop ran. With lanes = 1 or the host loop mode the searches run one
+ * after another on `stream`. Returns the first failing search's status
+ * (every search is run), BFS_CSR_EINVAL for a NULL or out-of-range argument.
+ * The level records of bfs_csr_level_stats are not kept for batch searches.
+ */
+int bfs_csr_run_batch(bfs_csr_handle h, int32_t num_sources, const int64_t *sources,
+                      int32_t *d_dist, int32_t *d_parent, int32_t *d_num_levels,
+                      int64_t *d_stamps, void *stream);
 
 /* Copy up to cap per-level records of the last synchronised run to host
  * memory; *count receives the number of levels the run had. */

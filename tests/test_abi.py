@@ -57,7 +57,7 @@ int main(void) {
   F(bfs_csr_options, max_depth); F(bfs_csr_options, validate); F(bfs_csr_options, block_threads);
   F(bfs_csr_options, grid_blocks); F(bfs_csr_options, barrier_timeout_ns);
   F(bfs_csr_options, test_unreachable_barrier); F(bfs_csr_options, push_beta);
-  F(bfs_csr_options, narrow_max_edges);
+  F(bfs_csr_options, narrow_max_edges); F(bfs_csr_options, lanes);
   F(bfs_csr_options, reserved);
   F(bfs_csr_level_stat, level); F(bfs_csr_level_stat, direction); F(bfs_csr_level_stat, advance);
   F(bfs_csr_level_stat, frontier); F(bfs_csr_level_stat, frontier_edges);
@@ -95,7 +95,7 @@ def test_defaults(fbc):
     assert (o.small_max_degree, o.cta_min_degree) == (32, 256)
     assert o.merge_path_min_frontier == 4096  # Gunrock paper's static hybrid threshold
     assert o.pull_alpha == 14.0 and o.push_beta == 24
-    assert o.max_depth == -1 and o.validate == 1
+    assert o.max_depth == -1 and o.validate == 1 and o.lanes == 1
     assert o.barrier_timeout_ns > 0 and o.test_unreachable_barrier == 0
 
 
@@ -108,6 +108,12 @@ def test_workspace_sizing(fbc):
     n = 1 << 20
     assert fbc.workspace_bytes(n, 16 * n, False) >= n * (8 + 16)
     assert fbc.workspace_bytes(n, 16 * n, True) >= n * (8 + 32)
+    # every lane adds one search part; the graph part (head array) is shared
+    one = fbc.workspace_bytes(n, 16 * n, False, fbc.default_options(lanes=1))
+    two = fbc.workspace_bytes(n, 16 * n, False, fbc.default_options(lanes=2))
+    three = fbc.workspace_bytes(n, 16 * n, False, fbc.default_options(lanes=3))
+    assert one < two < three and three - two == two - one and two - one < one
+    assert fbc.workspace_bytes(n, 16 * n, False, fbc.default_options(lanes=0)) == one
 
 
 def test_argument_checks_without_gpu(fbc):
@@ -126,6 +132,12 @@ def test_argument_checks_without_gpu(fbc):
     bad = fbc.default_options(block_threads=100)
     assert fbc.bfs_csr_workspace_bytes(10, 10, 0, ctypes.byref(bad), ctypes.byref(out)) == \
         fbc.BFS_CSR_EINVAL
+    for lanes in (-1, 9):
+        bad = fbc.default_options(lanes=lanes)
+        assert fbc.bfs_csr_workspace_bytes(10, 10, 0, ctypes.byref(bad), ctypes.byref(out)) == \
+            fbc.BFS_CSR_EINVAL
+    src = (ctypes.c_int64 * 1)(0)
+    assert fbc.bfs_csr_run_batch(None, 1, src, None, None, None, None, None) == fbc.BFS_CSR_EINVAL
     h = ctypes.c_void_p()
     assert fbc.bfs_csr_create(None, 1, 0, None, 0, None, 1, None, 0, None, None) == \
         fbc.BFS_CSR_EINVAL

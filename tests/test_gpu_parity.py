@@ -142,6 +142,32 @@ def test_corner_cases(fbc):
         check_against_oracle(fbc, g, srcs)
 
 
+def test_distances_past_the_hop_byte(fbc):
+    """Distances of 254 and more do not fit the one-byte hop code and go to
+    dist directly; here they are reached by push and by pull levels: a
+    300-vertex path ends in a dense random cluster (so the automatic rule
+    pulls at depth ~300), plus isolated vertices; every direction mode."""
+    rng = np.random.default_rng(17)
+    path = 300
+    cl = 4000
+    src = list(range(path - 1))
+    dst = list(range(1, path))
+    a = rng.integers(path, path + cl, 60000)
+    b = rng.integers(path, path + cl, 60000)
+    src += [path - 1] * 8 + a.tolist()
+    dst += rng.integers(path, path + cl, 8).tolist() + b.tolist()
+    g = graphgen.from_edges(path + cl + 50, src, dst, name="path_then_cluster")
+    for over in (dict(), dict(direction=1), dict(direction=2), dict(loop_mode=1)):
+        bfs = fbc.BfsCsr(_dev(g.row_ptr), _dev(g.col), symmetric=True,
+                         options=fbc.default_options(**over))
+        check_against_oracle(fbc, g, [150, path + 5, 0], bfs=bfs)  # source 0 last: its records
+        rec = bfs.level_stats()
+        if over.get("direction", 0) != 1:
+            assert any(r["direction"] == fbc.BFS_CSR_DIR_PULL and r["level"] >= 254
+                       for r in rec), over
+        bfs.close()
+
+
 def test_self_loops_and_duplicate_edges(fbc):
     rng = np.random.default_rng(5)
     src = rng.integers(0, 300, 3000)
@@ -387,6 +413,44 @@ def test_host_memory_batch(fbc):
             with pytest.raises(fbc.BfsError):
                 h.run_batch(bad, np.empty((len(bad), g.n), np.int32))
         h.close()
+
+
+def test_device_batch_on_concurrent_lanes(fbc):
+    """bfs_csr_run_batch: row i is source i's search whatever lane ran it
+    (1, 2 and 3 lanes, odd and even batch sizes, with and without parent),
+    equal to the oracle; the device stamps are ordered per search; the host
+    loop mode runs the batch one search at a time; bad arguments run
+    nothing."""
+    for cfg in (1, 3):
+        g = graphgen.config(cfg)
+        rp, col = _dev(g.row_ptr), _dev(g.col)
+        for lanes, extra in ((1, {}), (2, {}), (3, {}), (2, dict(loop_mode=1)),
+                             (2, dict(direction=2))):
+            bfs = fbc.BfsCsr(rp, col, True, options=fbc.default_options(lanes=lanes, **extra))
+            for k in (1, 5, 8):
+                srcs = [int(x) for x in g.sources[:k]][::-1]
+                dist = torch.full((k, g.n), -7, dtype=torch.int32, device="cuda")
+                par = torch.full((k, g.n), -7, dtype=torch.int32, device="cuda")
+                lev = torch.zeros(k, dtype=torch.int32, device="cuda")
+                stamps = torch.zeros(3 * k, dtype=torch.int64, device="cuda")
+                bfs.run_batch(srcs, dist, par if k != 5 else None, lev, stamps)
+                dist_h, par_h, lev_h = dist.cpu().numpy(), par.cpu().numpy(), lev.cpu().numpy()
+                st = stamps.cpu().numpy().reshape(k, 3)
+                for i, s in enumerate(srcs):
+                    want, _, want_levels = oracle.bfs(g.row_ptr, g.col, s, want_parent=False)
+                    assert np.array_equal(dist_h[i], want), (cfg, lanes, extra, k, i)
+                    assert lev_h[i] == want_levels
+                    if k != 5:
+                        assert oracle.check_parent(g.row_ptr, g.col, s, dist_h[i], par_h[i])[0] == 0
+                    else:
+                        assert (par_h[i] == -7).all()
+                    assert 0 < st[i, 0] <= st[i, 1] <= st[i, 2], (cfg, lanes, st[i])
+            # a single search on the same handle still works after a batch
+            check_against_oracle(fbc, g, g.sources[:2], bfs=bfs)
+            for bad in ([g.n], [-1]):
+                with pytest.raises(fbc.BfsError):
+                    bfs.run_batch(bad, torch.empty((1, g.n), dtype=torch.int32, device="cuda"))
+            bfs.close()
 
 
 def test_host_memory_api_new_csr_of_the_same_size(fbc):
