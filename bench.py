@@ -200,6 +200,22 @@ def algorithmic_bytes(torch, row_ptr, col, deg, src_of_edge, dist, stats, row_by
     return total, per_level
 
 
+def busy_time(intervals) -> float:
+    """Length of the union of [start, end] intervals: the time during which
+    at least one of them was running."""
+    busy, cur_a, cur_b = 0.0, None, None
+    for a, b in sorted(intervals):
+        if cur_b is None or a > cur_b:
+            if cur_b is not None:
+                busy += cur_b - cur_a
+            cur_a, cur_b = a, b
+        else:
+            cur_b = max(cur_b, b)
+    if cur_b is not None:
+        busy += cur_b - cur_a
+    return float(busy)
+
+
 def init_bytes(n: int, with_parent: bool = True) -> int:
     """The init kernel with bitmap discovery: one hop-code byte per vertex,
     parent (-1), the visited bitmap written and the dead bitmap read."""
@@ -330,19 +346,7 @@ def run_ours(args):
     runs = st.shape[0]
     init_ms = (st[:, 1] - st[:, 0]).tolist()
     level_ms = (st[:, 2] - st[:, 1]).tolist()
-    # Time during which at least one level loop ran (the union of the
-    # searches' level-loop intervals).
-    iv = sorted(zip(st[:, 1], st[:, 2]))
-    busy, cur_a, cur_b = 0.0, None, None
-    for a, b in iv:
-        if cur_b is None or a > cur_b:
-            if cur_b is not None:
-                busy += cur_b - cur_a
-            cur_a, cur_b = a, b
-        else:
-            cur_b = max(cur_b, b)
-    if cur_b is not None:
-        busy += cur_b - cur_a
+    busy = busy_time(zip(st[:, 1], st[:, 2]))
     edges_local = sum(per_source[s]["edges"] for s in sources) * args.steps
     edges_all = sum_over_ranks(torch, ws, float(edges_local), device)
     value = edges_all / (total_ms * 1e-3) / 1e9
