@@ -219,6 +219,32 @@ def test_config5_rmat25_sampled(fbc):
     bfs.close()
 
 
+def test_config5_rmat25_batch_on_two_lanes(fbc):
+    """The benchmark's launch configuration at full size: bfs_csr_run_batch
+    with two lanes over four sources; two rows against the oracle, two
+    certified by the invariant check; every parent row a valid BFS tree."""
+    g = graphgen.config(5)
+    bfs = fbc.BfsCsr(_dev(g.row_ptr), _dev(g.col), symmetric=True,
+                     options=fbc.default_options(lanes=2))
+    srcs = [int(s) for s in g.sources[:4]]
+    dist = torch.empty((4, g.n), dtype=torch.int32, device="cuda")
+    parent = torch.empty_like(dist)
+    levels = torch.empty(4, dtype=torch.int32, device="cuda")
+    bfs.run_batch(srcs, dist, parent, levels)
+    lev = levels.cpu().numpy()
+    for i, s in enumerate(srcs):
+        d = dist[i].cpu().numpy()
+        if i < 2:
+            want, _, want_levels = oracle.bfs(g.row_ptr, g.col, s, want_parent=False)
+            assert np.array_equal(d, want), i
+            assert lev[i] == want_levels
+        else:
+            assert oracle.check_dist(g.row_ptr, g.col, s, d)[0] == 0
+            assert lev[i] == int(d.max()) + 1
+        assert oracle.check_parent(g.row_ptr, g.col, s, d, parent[i].cpu().numpy())[0] == 0
+    bfs.close()
+
+
 # ---------------------------------------------------------------- option matrix
 
 OPTION_MATRIX = [
