@@ -292,6 +292,46 @@ def test_level_sizes_and_edges_walked():
     assert np.array_equal(sizes, np.bincount(dist[dist >= 0], minlength=nl))
 
 
+def test_edges_walked_pinned_to_the_worked_examples(golden):
+    """The walked-edge count (the TEPS numerator: CSR entries of the reached
+    vertices) on graphs where the pages or a closed form fix it.
+
+    ch. 22 section 22.1's six-vertex graph from source 0 reaches all six
+    vertices, so all 9 printed CSR entries are walked; cut at depth 2 (the
+    state the section prints after level 1) vertex 5 stays unreached but has
+    no out-edges, so still 9. PMPP 15.1's four-vertex graph is connected: 8
+    entries from every source. A path of m vertices walks 2(m - 1) entries
+    from any vertex; a graph of two components walks only the source's one.
+    """
+    gx = golden("six_vertex_directed.json")
+    rp, col = np.array(gx["row_ptr"]), np.array(gx["col"])
+    dist, _, _ = oracle.bfs(rp, col, gx["source"])
+    assert oracle.level_sizes(rp, dist)[3] == 9 == len(gx["col"])
+    d2, _, _ = oracle.bfs(rp, col, gx["source"], max_depth=gx["after_level_1"]["max_depth"])
+    assert oracle.level_sizes(rp, d2)[2:] == (5, 9)
+    # from vertex 3 only {3, 4, 5} are reached: rows of 2 + 1 + 0 entries
+    d3, _, _ = oracle.bfs(rp, col, 3)
+    assert oracle.level_sizes(rp, d3)[2:] == (3, 3)
+    g4 = golden("four_vertex_undirected.json")
+    rp4, col4 = np.array(g4["row_ptr"]), np.array(g4["col"])
+    for s in range(4):
+        d, _, _ = oracle.bfs(rp4, col4, s)
+        assert oracle.level_sizes(rp4, d)[2:] == (4, 8)
+    for m in (1, 2, 7, 100):
+        g = graphgen.path_graph(m)
+        for s in (0, m // 2, m - 1):
+            d, _, _ = oracle.bfs(g.row_ptr, g.col, s)
+            assert oracle.level_sizes(g.row_ptr, d)[2:] == (m, 2 * (m - 1))
+    # a 5-clique beside a 4-vertex path: 20 entries or 6
+    src = [a for a in range(5) for b in range(5) if a != b] + [5, 6, 7]
+    dst = [b for a in range(5) for b in range(5) if a != b] + [6, 7, 8]
+    g = graphgen.from_edges(9, src, dst)
+    assert g.nnz == 20 + 6
+    for s, want in ((0, (5, 20)), (4, (5, 20)), (5, (4, 6)), (8, (4, 6))):
+        d, _, _ = oracle.bfs(g.row_ptr, g.col, s)
+        assert oracle.level_sizes(g.row_ptr, d)[2:] == want
+
+
 def test_config1_eccentric_source_levels_equal_ecc_plus_one():
     g = graphgen.config(1)
     n = g.n
@@ -319,6 +359,10 @@ MUTANTS = [
      "if (max_depth >= 0 && dist[u] > max_depth)"),              # off-by-one depth bound
     ("e < last; ++e) {\n            const int32_t w = col[e];\n            if (dist[w] == -1)",
      "e + 1 < last; ++e) {\n            const int32_t w = col[e];\n            if (dist[w] == -1)"),
+    ("edges += row_at(row_ptr, row_ptr_64, v + 1) -",
+     "edges += row_at(row_ptr, row_ptr_64, v + 1) + 0 *"),  # walked count without the row start
+    ("row_at(row_ptr, row_ptr_64, v);\n        if (d > deepest)",
+     "row_at(row_ptr, row_ptr_64, 0);\n        if (d > deepest)"),  # wrong row start
 ]
 
 
@@ -350,6 +394,9 @@ def test_pins_reject_oracle_mutants(old, new, golden, monkeypatch):
             "for s, want in g4['dist_from'].items():\n"
             "    d, p, L = oracle.bfs(np.array(g4['row_ptr']), np.array(g4['col']), int(s))\n"
             "    ok = ok and d.tolist() == want and L == max(want) + 1\n"
+            "    ok = ok and oracle.level_sizes(np.array(g4['row_ptr']), d)[3] == 8\n"
+            "d3, _, _ = oracle.bfs(rp, col, 3)\n"
+            "ok = ok and oracle.level_sizes(rp, d3)[2:] == (3, 3)\n"
             "print('PASS' if ok else 'FAIL')\n" % (tmp, gdir, gdir))
         out = subprocess.run(["python", "-c", code], capture_output=True, text=True,
                              timeout=120)
