@@ -926,6 +926,8 @@ extern "C" int bfs_csr_run_noalloc(int64_t n, int64_t nnz, const int32_t* d_row_
         return rc;
     if (h.opt.direction == BFS_CSR_DIR_PULL && !h.symmetric)
         return BFS_CSR_EUNSUPPORTED;
+    if (h.opt.lanes > 1)
+        return BFS_CSR_EUNSUPPORTED;  // the scratch array holds one search's state
     void* scratch = nullptr;
     rc = noalloc_scratch(h.device, &scratch);
     if (rc != BFS_CSR_OK)

@@ -108,6 +108,11 @@ typedef struct bfs_csr_level_stat {
     int64_t unvisited;       /* non-isolated vertices not yet reached at level start */
     int64_t max_degree;      /* largest out-degree in F_k */
     int64_t t_start_ns;      /* device global timer at the level's start */
+    int64_t t_work_ns;       /* device global timer when the last CTA finished the
+                                level's work, before the barrier that ends it
+                                (t_work_ns - t_start_ns is the level's busy time;
+                                the rest, up to the next level's start, is its
+                                synchronisation cost) */
 } bfs_csr_level_stat;
 
 typedef struct bfs_csr_t *bfs_csr_handle;
@@ -274,10 +279,13 @@ int bfs_csr_last_cuda_error(bfs_csr_handle h);
  * search's status (*num_levels, when not NULL, receives the level count on
  * the host). The first call on a device looks up the scratch array's device
  * address (cudaGetSymbolAddress) with that device current; make that first
- * call before any stream capture. Every call shares the one scratch array
- * and resets the parts that must start from zero; calls that overlap on the
- * GPU (from two host threads or two streams) race on it and must not be
- * issued.
+ * call before any stream capture. The address is kept for the life of the
+ * process: after a cudaDeviceReset of that device this entry point must not
+ * be called again in the same process. Every call shares the one scratch
+ * array and resets the parts that must start from zero; calls that overlap
+ * on the GPU (from two host threads or two streams) race on it and must not
+ * be issued. One search at a time: opt->lanes above 1 gives
+ * BFS_CSR_EUNSUPPORTED.
  */
 #define BFS_CSR_NOALLOC_MAX_VERTICES 1048576
 int bfs_csr_run_noalloc(int64_t n, int64_t nnz, const int32_t *d_row_ptr,

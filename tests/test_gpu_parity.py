@@ -6,6 +6,9 @@ trees are correct); the level count and the per-level frontier sizes must
 equal the oracle's (the sizes summing to the reached count is the gate that
 catches a vertex queued twice, "100 Days of GPU, Day 38", "Pitfalls").
 """
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 import pytest
 
@@ -60,6 +63,47 @@ def check_against_oracle(fbc, g, sources, bfs=None, max_depth=-1, stats=True):
             assert sum(got) == reached
     if own:
         bfs.close()
+
+
+def check_rows_against_oracle(g, srcs, dist_rows, parent_rows, levels):
+    """Row i of dist_rows/parent_rows (host arrays) and levels[i] are source
+    srcs[i]'s search. Every row is compared element by element with the
+    oracle's distances and every parent row is tree-checked; the oracle runs
+    for several sources at once (its ctypes calls release the GIL)."""
+    def one(i):
+        s = int(srcs[i])
+        want, _, want_levels = oracle.bfs(g.row_ptr, g.col, s, want_parent=False)
+        d = dist_rows[i]
+        bad = np.nonzero(d != want)[0]
+        first = (int(bad[0]), int(d[bad[0]]), int(want[bad[0]])) if bad.size else None
+        pcode, pwhere = (oracle.check_parent(g.row_ptr, g.col, s, d, parent_rows[i])
+                         if parent_rows is not None else (0, -1))
+        return s, bad.size, first, int(levels[i]), want_levels, pcode, pwhere
+
+    workers = max(1, min(16, os.cpu_count() or 1, len(srcs)))
+    with ThreadPoolExecutor(max_workers=workers) as ex:
+        results = list(ex.map(one, range(len(srcs))))
+    for s, nbad, first, lev, want_levels, pcode, pwhere in results:
+        assert nbad == 0, "%s source %d: dist differs at %d vertices, first (v, gpu, oracle) %s" % (
+            g.name, s, nbad, first)
+        assert lev == want_levels, (g.name, s, lev, want_levels)
+        assert pcode == 0, "%s source %d: invalid parent at %d" % (g.name, s, pwhere)
+
+
+def run_batch_rows(fbc, g, srcs, lanes, **over):
+    """bfs_csr_run_batch over srcs on `lanes` lanes; host copies of the rows."""
+    bfs = fbc.BfsCsr(_dev(g.row_ptr), _dev(g.col), symmetric=g.symmetric,
+                     options=fbc.default_options(lanes=lanes, **over))
+    k = len(srcs)
+    dist = torch.empty((k, g.n), dtype=torch.int32, device="cuda")
+    parent = torch.empty_like(dist)
+    levels = torch.empty(k, dtype=torch.int32, device="cuda")
+    bfs.run_batch([int(s) for s in srcs], dist, parent, levels)
+    out = dist.cpu().numpy(), parent.cpu().numpy(), levels.cpu().numpy()
+    bfs.close()
+    del dist, parent, levels
+    torch.cuda.empty_cache()
+    return out
 
 
 # ---------------------------------------------------------------- goldens
@@ -198,51 +242,43 @@ def test_config1_all_sources(fbc):
     check_against_oracle(fbc, g, [best] + list(g.sources))
 
 
-@pytest.mark.parametrize("cfg,count", [(2, 6), (3, 6), (4, 1)])
-def test_configs_2_to_4(fbc, cfg, count):
+@pytest.mark.parametrize("cfg", [2, 3])
+def test_configs_2_and_3_every_source(fbc, cfg):
+    """All 64 sources of the uniform random graph and of R-MAT scale 22: the
+    batch path on two lanes (the benchmark's configuration) element by
+    element against the oracle, every parent row tree-checked; the first
+    six also through single runs with their per-level records."""
     g = graphgen.config(cfg)
-    check_against_oracle(fbc, g, g.sources[:count])
+    assert len(g.sources) == 64
+    check_against_oracle(fbc, g, g.sources[:6])
+    dist, parent, levels = run_batch_rows(fbc, g, g.sources, lanes=2)
+    check_rows_against_oracle(g, g.sources, dist, parent, levels)
 
 
-def test_config5_rmat25_sampled(fbc):
+def test_config4_grid_corner(fbc):
+    g = graphgen.config(4)
+    check_against_oracle(fbc, g, g.sources[:1])
+    dist, parent, levels = run_batch_rows(fbc, g, g.sources[:1], lanes=1)
+    check_rows_against_oracle(g, g.sources[:1], dist, parent, levels)
+
+
+def test_config5_rmat25_single_runs(fbc):
+    """R-MAT scale 25 (int64 row_ptr) through single runs: dist, parent,
+    level count and per-level records of two sources against the oracle."""
     g = graphgen.config(5)
     assert g.row_ptr.dtype == np.int64 and g.n == 1 << 25
-    bfs = fbc.BfsCsr(_dev(g.row_ptr), _dev(g.col), symmetric=True)
-    check_against_oracle(fbc, g, g.sources[:2], bfs=bfs)
-    # the remaining sources: distances certified by the invariant check
-    for s in g.sources[2:6]:
-        dist, parent, levels = bfs.search(int(s))
-        d = dist.cpu().numpy()
-        assert oracle.check_dist(g.row_ptr, g.col, int(s), d)[0] == 0
-        assert oracle.check_parent(g.row_ptr, g.col, int(s), d, parent.cpu().numpy())[0] == 0
-        assert levels == int(d.max()) + 1
-    bfs.close()
+    check_against_oracle(fbc, g, g.sources[:2])
 
 
-def test_config5_rmat25_batch_on_two_lanes(fbc):
-    """The benchmark's launch configuration at full size: bfs_csr_run_batch
-    with two lanes over four sources; two rows against the oracle, two
-    certified by the invariant check; every parent row a valid BFS tree."""
+def test_config5_rmat25_every_source_on_two_lanes(fbc):
+    """The benchmark's step at full size: bfs_csr_run_batch with two lanes
+    over all 16 sources of R-MAT scale 25; every dist row equal to the
+    oracle's element by element, every parent row a valid BFS tree, every
+    level count equal to the oracle's."""
     g = graphgen.config(5)
-    bfs = fbc.BfsCsr(_dev(g.row_ptr), _dev(g.col), symmetric=True,
-                     options=fbc.default_options(lanes=2))
-    srcs = [int(s) for s in g.sources[:4]]
-    dist = torch.empty((4, g.n), dtype=torch.int32, device="cuda")
-    parent = torch.empty_like(dist)
-    levels = torch.empty(4, dtype=torch.int32, device="cuda")
-    bfs.run_batch(srcs, dist, parent, levels)
-    lev = levels.cpu().numpy()
-    for i, s in enumerate(srcs):
-        d = dist[i].cpu().numpy()
-        if i < 2:
-            want, _, want_levels = oracle.bfs(g.row_ptr, g.col, s, want_parent=False)
-            assert np.array_equal(d, want), i
-            assert lev[i] == want_levels
-        else:
-            assert oracle.check_dist(g.row_ptr, g.col, s, d)[0] == 0
-            assert lev[i] == int(d.max()) + 1
-        assert oracle.check_parent(g.row_ptr, g.col, s, d, parent[i].cpu().numpy())[0] == 0
-    bfs.close()
+    assert len(g.sources) == 16
+    dist, parent, levels = run_batch_rows(fbc, g, g.sources, lanes=2)
+    check_rows_against_oracle(g, g.sources, dist, parent, levels)
 
 
 # ---------------------------------------------------------------- option matrix

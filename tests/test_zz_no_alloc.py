@@ -32,7 +32,7 @@ def fbc():
     return frontier_bfs_csr_gb300
 
 
-def _noalloc(fbc, row_ptr, col, n, nnz, source, symmetric=True, want_parent=True):
+def _noalloc(fbc, row_ptr, col, n, nnz, source, symmetric=True, want_parent=True, opt=None):
     dist = torch.full((n,), -7, dtype=torch.int32, device="cuda")
     parent = torch.full((n,), -7, dtype=torch.int32, device="cuda") if want_parent else None
     dlev = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -42,17 +42,20 @@ def _noalloc(fbc, row_ptr, col, n, nnz, source, symmetric=True, want_parent=True
                                      col.data_ptr() if nnz else None, int(symmetric),
                                      int(source), dist.data_ptr(),
                                      parent.data_ptr() if want_parent else None,
-                                     dlev.data_ptr(), ctypes.byref(hlev), None, stream)
+                                     dlev.data_ptr(), ctypes.byref(hlev),
+                                     ctypes.byref(opt) if opt is not None else None, stream)
     return status, dist, parent, int(hlev.value), int(dlev.item())
 
 
-def _compare(fbc, g, sources):
+def _compare(fbc, g, sources, **over):
     rp = torch.from_numpy(g.row_ptr).cuda()
     col = torch.from_numpy(g.col).cuda()
-    ref = fbc.BfsCsr(rp, col, symmetric=g.symmetric)
+    opt = fbc.default_options(**over) if over else None
+    ref = fbc.BfsCsr(rp, col, symmetric=g.symmetric, options=opt)
     for s in sources:
         s = int(s)
-        status, dist, parent, hlev, dlev = _noalloc(fbc, rp, col, g.n, g.nnz, s, g.symmetric)
+        status, dist, parent, hlev, dlev = _noalloc(fbc, rp, col, g.n, g.nnz, s, g.symmetric,
+                                                    opt=opt)
         assert status == fbc.BFS_CSR_OK, fbc.bfs_csr_status_string(status)
         want_dist, _, want_levels = ref.search(s)
         assert torch.equal(dist, want_dist)
@@ -94,3 +97,31 @@ def test_noalloc_rejects_sizes_beyond_the_limit(fbc):
     assert status == fbc.BFS_CSR_EUNSUPPORTED
     status, *_ = _noalloc(fbc, rp, col, 10, 0, 10)    # source out of range
     assert status == fbc.BFS_CSR_EINVAL
+
+
+@pytest.mark.parametrize("over", [dict(loop_mode=1, discovery=1), dict(direction=2),
+                                  dict(direction=1, advance=2, discovery=1)],
+                         ids=["host_loop+cas", "pull", "push+merge_path+cas"])
+def test_noalloc_options_match_regular_entry_point(fbc, over):
+    """The host level loop, CAS discovery (dist written at discovery instead
+    of through the hop codes) and forced directions on the shared scratch,
+    each against the regular entry point with the same options."""
+    g = graphgen.config(1)
+    _compare(fbc, g, g.sources[:2], **over)
+
+
+def test_noalloc_malformed_csr_then_recovers(fbc):
+    """A malformed CSR is rejected by the validation pass with EINVAL; the
+    next call on a good graph, on the same shared scratch, is still right.
+    Several lanes are refused: the scratch holds one search."""
+    g = graphgen.config(1)
+    bad = g.row_ptr.copy()
+    bad[10], bad[11] = bad[11], bad[10] - 1      # row_ptr decreases
+    rp_bad = torch.from_numpy(bad).cuda()
+    col = torch.from_numpy(g.col).cuda()
+    status, *_ = _noalloc(fbc, rp_bad, col, g.n, g.nnz, int(g.sources[0]))
+    assert status == fbc.BFS_CSR_EINVAL
+    status, *_ = _noalloc(fbc, torch.from_numpy(g.row_ptr).cuda(), col, g.n, g.nnz,
+                          int(g.sources[0]), opt=fbc.default_options(lanes=2))
+    assert status == fbc.BFS_CSR_EUNSUPPORTED
+    _compare(fbc, g, g.sources[2:4])
