@@ -13,11 +13,15 @@ GTEPS counts, per search, the CSR entries of the reached vertices (the sum of
 their out-degrees, "edges to walk" in the Day 38 level table); the same
 count halved (undirected edges) is reported beside it.
 
-Roofline: the level loops' algorithmic bytes (the byte model in
-`algorithmic_bytes`, replayed from each search's own distances and level
-directions) over the time during which at least one level loop ran (from
-device timer stamps the library records per search), against the measured
-HBM copy bandwidth.
+Roofline: the algorithmic bytes of the level loops -- what each level's
+chosen step must touch, replayed exactly from each search's own distances
+and level directions (`survey_bytes`: queue, row offsets, col and one probe
+word per scanned entry, dist + parent of the discovered vertices, the next
+queue or bitmap) -- over the time during which at least one level loop ran
+(device timer stamps the library records per search), against the measured
+HBM copy bandwidth. The kernel's own bookkeeping beyond that (queue row
+starts and degree prefixes, representation switches, the end-of-search dist
+pass) is counted apart (`kernel_extra_bytes`).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Under torchrun (N > 1) every rank runs an independent replica on its GPU
@@ -52,6 +56,17 @@ WORKLOADS = {
     1: "powerlaw_3485: Chung-Lu power-law graph, 3,485 vertices; 64 sources (seed 0)",
 }
 
+# The pages' own figures, quoted as context only (other hardware, other graph).
+PAGES_CONTEXT = {
+    "hardware": "Tesla T4 (sm_75, 40 SMs); 3,485-word graph, 31,812 CSR entries, 10 levels",
+    "whole_bfs_ms": {"thread_per_vertex": 1.8091, "warp_per_vertex": 0.3340},
+    "isolated_level_walk_x64_ms": {"level_4": [1.3724, 0.0881], "level_5": [1.0068, 0.0796],
+                                   "level_6": [0.1172, 0.0485]},
+    "lane_slots_thread_per_vertex": 251872, "useful_edges": 31758,
+    "launches": "10 launches for 10 levels; 5-10 us per launch stated (PMPP ch. 15 notes)",
+    "source": "100 Days of GPU, Day 38 'Results'; PMPP ch. 15 notes section 15.7",
+}
+
 
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -61,6 +76,14 @@ def measured_peaks():
         return float(d["hbm_gbs"]), "measured"
     except (OSError, KeyError, ValueError):
         return 6800.0, "fallback"
+
+
+def host_cores():
+    try:
+        aff = len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        aff = None
+    return {"online": os.cpu_count(), "affinity": aff}
 
 
 # ------------------------------------------------------------------ clocks
@@ -125,79 +148,117 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-# ------------------------------------------------------------------ byte model
+# ------------------------------------------------------------------ byte models
 
-def algorithmic_bytes(torch, row_ptr, col, deg, src_of_edge, dist, stats, row_bytes):
-    """Bytes the level kernel must touch, replayed from one search.
+def level_counts(torch, row_ptr64, col, deg, src_of_edge, dist, stats):
+    """Exact per-level counts of one search, replayed on the device from its
+    distances and the direction each level took.
 
-    row_ptr, col, deg, src_of_edge: device tensors of the graph (int64 row_ptr
-    and degrees, int32 col and per-entry source). dist: the search's output.
-    stats: its per-level records. Push level k (queue Q_k = frontier vertices
-    with out-degree > 0, N_k = vertices at distance k + 1, N'_k those of them
-    with edges): queue entries read (4 + 2R) |Q_k|, col 4 m_F, one visited word
-    per edge 4 m_F, row offsets of each discovered vertex 2R |N_k|, dist and
-    parent 8 |N_k|, its visited word 4 |N_k|, queue entries written (4 + 2R)
-    |N'_k|. Pull level k (U'_k = unreached vertices of nonzero degree, c_k =
-    entries scanned: up to and including the first neighbour at distance k for
-    the vertices found, the whole row for the others): visited bitmap n/8,
-    row offsets 2R |U'_k|, col 4 c_k, one frontier-bitmap word per scanned
-    entry 4 c_k, dist and parent 8 |N_k|, next-frontier bitmap n/8, visited
-    words with a discovery 4 per word. Representation switches: queue to bitmap
-    n/8 + 8 |Q_k|; bitmap to queue n/8 + 2R |F_k| + (4 + 2R) |Q_k|. Output:
-    the -1 of every unreached vertex's dist, 4 (n - reached), written by the
-    level kernel when the search ends (the reached vertices' dist bytes are
-    counted at their discovery above).
+    Per level k: F = |{v: dist v = k}|, Q = those with out-edges, mF = their
+    out-degree sum, N = |{v: dist v = k + 1}| (the vertices level k
+    discovers), Ne = those with out-edges, U = vertices of nonzero degree not
+    reached by level k (unvisited at its start). Pull levels also get c = the
+    CSR entries a bottom-up scan reads: for each vertex it finds, its row up
+    to and including the first neighbour at distance k; for every other
+    vertex of U, its whole row; and tw = 32-vertex words holding a find.
     """
-    n = int(dist.numel())
-    R = row_bytes
-    words = (n + 31) // 32
     has_edges = deg > 0
-    total = 0
-    prev = DIR_PUSH
-    per_level = []
-    dist_src = None
+    out = []
+    ds = dd = None
     for k, st in enumerate(stats):
         in_k = dist == k
         nxt = dist == (k + 1)
-        Fk = int(in_k.sum().item())
-        Qk = int((in_k & has_edges).sum().item())
-        Nk = int(nxt.sum().item())
-        Nk_e = int((nxt & has_edges).sum().item())
-        mF = int(deg[in_k].sum().item())
-        b = 0
+        c = {"level": k, "direction": st["direction"], "advance": st["advance"],
+             "F": int(in_k.sum().item()), "Q": int((in_k & has_edges).sum().item()),
+             "mF": int(deg[in_k].sum().item()), "N": int(nxt.sum().item()),
+             "Ne": int((nxt & has_edges).sum().item()),
+             "U": int((((dist < 0) | (dist > k)) & has_edges).sum().item()), "c": 0, "tw": 0}
         if st["direction"] == DIR_PULL:
-            if prev == DIR_PUSH:
-                b += words * 4 + 8 * Qk
-            unreached = ((dist < 0) | (dist > k)) & has_edges
-            Uk = int(unreached.sum().item())
-            if dist_src is None:
-                dist_src = dist[src_of_edge.long()]
-            dist_dst = dist[col.long()]
-            hit = (dist_src == k + 1) & (dist_dst == k)
+            if ds is None:
+                ds = dist[src_of_edge.long()]
+                dd = dist[col.long()]
+            hit = (ds == k + 1) & (dd == k)
             pos = torch.nonzero(hit).squeeze(1)
-            first = torch.full((n,), -1, dtype=torch.int64, device=dist.device)
+            found = 0
             if pos.numel():
                 owner = src_of_edge[pos].long()
-                big = torch.full((n,), np.iinfo(np.int64).max, dtype=torch.int64,
+                big = torch.full((dist.numel(),), np.iinfo(np.int64).max, dtype=torch.int64,
                                  device=dist.device)
                 big.scatter_reduce_(0, owner, pos, reduce="amin")
-                found = nxt & has_edges
-                first = torch.where(found, big - row_ptr[:-1], first)
-            scanned_found = int((first[nxt] + 1).sum().item()) if Nk else 0
-            not_found = unreached & ~nxt
-            scanned_rest = int(deg[not_found].sum().item())
-            c = scanned_found + scanned_rest
-            touched_words = int(torch.unique(torch.nonzero(nxt).squeeze(1) // 32).numel()) if Nk else 0
-            b += words * 4 + 2 * R * Uk + 4 * c + 4 * c + 8 * Nk + words * 4 + 4 * touched_words
-        else:
-            if prev == DIR_PULL:
-                b += words * 4 + 2 * R * Fk + (4 + 2 * R) * Qk
-            b += (4 + 2 * R) * Qk + 4 * mF + 4 * mF + 2 * R * Nk + 8 * Nk + 4 * Nk + (4 + 2 * R) * Nk_e
-        per_level.append(b)
-        total += b
-        prev = st["direction"]
-    total += 4 * int((dist < 0).sum().item())
-    return total, per_level
+                sel = nxt & has_edges
+                found = int((big[sel] - row_ptr64[:-1][sel] + 1).sum().item())
+                del big, owner
+            rest = ((dist < 0) | (dist > k + 1)) & has_edges
+            c["c"] = found + int(deg[rest].sum().item())
+            if c["N"]:
+                c["tw"] = int(torch.unique(torch.nonzero(nxt).squeeze(1) // 32).numel())
+            del hit, pos
+        out.append(c)
+    return out
+
+
+def survey_bytes(c, n: int, R: int) -> int:
+    """Algorithmic bytes of one level: what the chosen step itself must touch.
+    Top-down: the queue 4|F|, row offsets 2R|F|, col 4 m_F, one probe word per
+    edge 4 m_F, dist + parent of the discovered vertices 8|N|, the next queue
+    4|N| and bitmap |N|/8. Bottom-up: the visited bitmap n/8, row offsets
+    2R|U|, col 4c and one frontier-bitmap word per scanned entry 4c, dist +
+    parent 8|N|, the next-frontier bitmap n/8. Random single-word probes are
+    counted at their word size."""
+    if c["direction"] == DIR_PULL:
+        return n // 8 + 2 * R * c["U"] + 8 * c["c"] + 8 * c["N"] + n // 8
+    F, N = c["F"], c["N"]
+    return 4 * F + 2 * R * F + 8 * c["mF"] + 8 * N + 4 * N + N // 8
+
+
+def kernel_bytes(c, prev_dir: int, n: int, R: int) -> int:
+    """The same level as this library's kernel touches it, single words at
+    their size: a queue entry is (vertex, row start, degree prefix), so queue
+    reads and writes are (4 + 2R) per vertex with out-edges and every winner's
+    row offsets are read once (2R); a switch between the representations
+    costs a bitmap pass (and the queue build reads row offsets); a pull level
+    also rewrites the visited words that gained a vertex."""
+    words = (n + 31) // 32
+    F, Q, N, Ne = c["F"], c["Q"], c["N"], c["Ne"]
+    b = 0
+    if c["direction"] == DIR_PULL:
+        if prev_dir == DIR_PUSH:
+            b += 4 * words + 8 * Q
+        b += 4 * words + 2 * R * c["U"] + 8 * c["c"] + 8 * N + 4 * words + 4 * c["tw"]
+    else:
+        if prev_dir == DIR_PULL:
+            b += 4 * words + 2 * R * F + (4 + 2 * R) * Q
+        b += (4 + 2 * R) * Q + 8 * c["mF"] + 2 * R * N + 8 * N + 4 * N + (4 + 2 * R) * Ne
+    return b
+
+
+def search_bytes(counts, n: int, R: int, reached: int):
+    """(survey bytes, kernel bytes, survey bytes per level) of one search's
+    level loop. The kernel also writes every unreached vertex's -1 at the
+    end (4 (n - reached); the reached vertices' dist is counted at their
+    discovery)."""
+    prev = DIR_PUSH
+    s_tot, k_tot, per = 0, 0, []
+    for c in counts:
+        sb = survey_bytes(c, n, R)
+        per.append(sb)
+        s_tot += sb
+        k_tot += kernel_bytes(c, prev, n, R)
+        prev = c["direction"]
+    return s_tot, k_tot + 4 * (n - reached), per
+
+
+def init_bytes_survey(n: int) -> int:
+    """Init per the scope table: dist and parent filled (8n), two bitmaps
+    cleared (n/4)."""
+    return 8 * n + n // 4
+
+
+def init_bytes_kernel(n: int, with_parent: bool = True) -> int:
+    """This library's init kernel with bitmap discovery: one hop-code byte per
+    vertex, parent (-1), the visited bitmap written and the dead bitmap read."""
+    words = (n + 31) // 32
+    return (n + 15) // 16 * 16 + (4 * n if with_parent else 0) + 8 * words
 
 
 def busy_time(intervals) -> float:
@@ -216,11 +277,12 @@ def busy_time(intervals) -> float:
     return float(busy)
 
 
-def init_bytes(n: int, with_parent: bool = True) -> int:
-    """The init kernel with bitmap discovery: one hop-code byte per vertex,
-    parent (-1), the visited bitmap written and the dead bitmap read."""
-    words = (n + 31) // 32
-    return (n + 15) // 16 * 16 + (4 * n if with_parent else 0) + 8 * words
+def graph_tensors(torch, g, device):
+    row_ptr = torch.from_numpy(g.row_ptr).to(device)
+    col = torch.from_numpy(g.col).to(device)
+    row64 = row_ptr.to(torch.int64)
+    deg = torch.diff(row64)
+    return row_ptr, col, row64, deg
 
 
 # ------------------------------------------------------------------ distributed
@@ -282,39 +344,45 @@ def run_ours(args):
         g = graphgen.config(args.config)
     all_sources = g.sources[:args.sources] if args.sources > 0 else g.sources
     sources = rank_sources(all_sources, rank, ws)
-    row_ptr = torch.from_numpy(g.row_ptr).to(device)
-    col = torch.from_numpy(g.col).to(device)
+    row_ptr, col, row64, deg = graph_tensors(torch, g, device)
     R = 8 if g.row_ptr_64 else 4
     bfs = fbc.BfsCsr(row_ptr, col, symmetric=True,
                      options=fbc.default_options(lanes=args.lanes))
     n = g.n
-    dist = torch.empty(n, dtype=torch.int32, device=device)
-    parent = torch.empty(n, dtype=torch.int32, device=device)
-    deg = torch.diff(row_ptr.to(torch.int64))
+    k = len(sources)
     stream = torch.cuda.current_stream(device)
 
-    # Untimed pass over every source: warms the kernels and records, per
-    # source, the walked-edge count, the level records and the byte model.
-    src_of_edge = torch.repeat_interleave(torch.arange(n, device=device, dtype=torch.int32),
-                                          deg)
+    # Untimed pass, one bfs_csr_run per source on the whole GPU: warms the
+    # kernels and records, per source, the walked-edge count, the level
+    # records, the replayed byte counts and the outputs (for the consistency
+    # check of the timed batch).
+    src_of_edge = torch.repeat_interleave(torch.arange(n, device=device, dtype=torch.int32), deg)
+    ref_dist = torch.empty((k, n), dtype=torch.int32, device=device)
+    ref_levels = []
     per_source = {}
-    for s in sources:
+    parent = torch.empty(n, dtype=torch.int32, device=device)
+    for i, s in enumerate(sources):
+        dist = ref_dist[i]
         bfs.run(s, dist, parent, stream=stream)
         levels = bfs.sync(stream)
-        reached = dist >= 0
-        edges = int(deg[reached].sum().item())
+        ref_levels.append(levels)
+        reached_mask = dist >= 0
+        reached = int(reached_mask.sum().item())
+        edges = int(deg[reached_mask].sum().item())
         stats = bfs.level_stats()
-        lb, per_level = algorithmic_bytes(torch, row_ptr.to(torch.int64), col, deg, src_of_edge,
-                                          dist, stats, R)
+        counts = level_counts(torch, row64, col, deg, src_of_edge, dist, stats)
+        sb, kb, per = search_bytes(counts, n, R, reached)
         torch.cuda.empty_cache()
-        per_source[s] = {"levels": levels, "edges": edges, "level_bytes": lb,
+        per_source[s] = {"levels": levels, "edges": edges, "survey_bytes": sb, "kernel_bytes": kb,
                          "directions": "".join("P" if x["direction"] == DIR_PUSH else "U"
-                                               for x in stats),
-                         "per_level_bytes": per_level}
+                                               for x in stats)}
+        if i == 0:
+            table = per_level_table(counts, per, stats, peak)
     del src_of_edge
+    torch.cuda.empty_cache()
+
     # Timed step: one bfs_csr_run_batch over the batch of sources (the searches
     # run on `lanes` lanes at once); dist/parent rows per source.
-    k = len(sources)
     dist_b = torch.empty((k, n), dtype=torch.int32, device=device)
     parent_b = torch.empty((k, n), dtype=torch.int32, device=device)
     levels_b = torch.empty(k, dtype=torch.int32, device=device)
@@ -339,8 +407,12 @@ def run_ours(args):
     clocks = sampler.stop()
     local_ms = t0.elapsed_time(t1)
     total_ms = max_over_ranks(torch, ws, local_ms, device)
-    # The last step's outputs against the untimed pass (same searches).
-    status_ok = bool(torch.equal(dist_b[-1], dist)) if k else True
+    # Every row of the last timed step against the untimed single runs (the
+    # CUDA path against itself: the oracle certifies the rows below).
+    repeat_ok = bool(torch.equal(dist_b, ref_dist)) and \
+        levels_b.cpu().tolist() == ref_levels
+    del ref_dist
+    torch.cuda.empty_cache()
 
     st = stamps.cpu().numpy().reshape(-1, 3).astype(np.float64) * 1e-6   # ms
     runs = st.shape[0]
@@ -351,10 +423,12 @@ def run_ours(args):
     edges_all = sum_over_ranks(torch, ws, float(edges_local), device)
     value = edges_all / (total_ms * 1e-3) / 1e9
 
-    lvl_bytes = sum(per_source[s]["level_bytes"] for s in sources) * args.steps
+    lvl_bytes = sum(per_source[s]["survey_bytes"] for s in sources) * args.steps
+    ker_bytes = sum(per_source[s]["kernel_bytes"] for s in sources) * args.steps
     achieved = lvl_bytes / (busy * 1e-3) / 1e9
-    init_b = init_bytes(n) * runs
+    init_b = init_bytes_kernel(n) * runs
     init_gbs = init_b / (sum(init_ms) * 1e-3) / 1e9
+    run_bytes = (lvl_bytes + init_bytes_survey(n) * runs) / args.steps
 
     result = {
         "metric": METRIC, "value": round(value, 3), "unit": "GTEPS", "n_gpus": ws,
@@ -380,32 +454,85 @@ def run_ours(args):
                      "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_kind": peak_kind, "traffic": None,
+                     "traffic_source": None,
                      "algorithmic_bytes_per_launch": int(lvl_bytes / runs),
+                     "byte_model": "scope-table level bytes (bench.py survey_bytes), replayed "
+                                   "from each search's distances and directions",
+                     "kernel_extra_bytes_per_launch": int((ker_bytes - lvl_bytes) / runs),
                      "launch_ms_mean": round(sum(level_ms) / runs, 4),
                      "level_kernel_busy_ms": round(busy, 4),
                      "timing": "device timer stamps per search; achieved = algorithmic bytes "
                                "of every level-loop launch / time any level loop ran"},
+        "run_roofline": {"bytes_per_step": int(run_bytes),
+                         "achieved_gbs": round(run_bytes / (total_ms / args.steps * 1e-3) / 1e9, 1),
+                         "frac": round(run_bytes / (total_ms / args.steps * 1e-3) / 1e9 / peak, 4),
+                         "what": "init (8n + n/4) plus level bytes per step over the step time"},
+        "per_level": table,
         "init_kernel": {"achieved_gbs": round(init_gbs, 1), "frac": round(init_gbs / peak, 4),
-                        "bytes_per_launch": init_bytes(n), "launch_ms_mean": round(sum(init_ms) / runs, 4)},
+                        "bytes_per_launch": init_bytes_kernel(n),
+                        "launch_ms_mean": round(sum(init_ms) / runs, 4)},
         "clocks": clocks,
         "gpu_launches": 2 * runs,
-        "status_after_timing": "ok" if status_ok else "error",
+        "repeat_consistent": repeat_ok,
+        "status_after_timing": "not certified (--no-cpu)",
     }
     traffic = read_traffic_summary(args.config)
     if traffic is not None:
         result["roofline"]["traffic"] = traffic
+        result["roofline"]["traffic_source"] = ("committed ncu summary "
+                                                "profiles/level_kernel_rmat25_traffic.txt "
+                                                "(dram__bytes_read.sum + dram__bytes_write.sum "
+                                                "per launch, same kernel source)")
+    timed_rows = None
+    if rank == 0 and not args.no_cpu:
+        timed_rows = (list(sources), dist_b.cpu().numpy(), parent_b.cpu().numpy(),
+                      levels_b.cpu().numpy())
     bfs.close()
+    del dist_b, parent_b, stamps, bfs
+    torch.cuda.empty_cache()
 
+    config_rows = {}
+    if rank == 0 and not args.no_configs:
+        result["per_config"] = per_config(torch, fbc, graphgen, device, peak, config_rows,
+                                          keep_rows=not args.no_cpu)
+    if rank == 0 and not args.no_ablation:
+        cases = [(2, None), (3, None)] + ([(5, g)] if args.config == 5 else [])
+        result["ablation"] = ablation(torch, fbc, graphgen, device, cases)
     if rank == 0 and not args.no_overhead:
         result["per_level_overhead_us"] = per_level_overhead(torch, fbc, graphgen, device)
     if not args.no_e2e:
         result["e2e"] = run_e2e(torch, fbc, g, sources, args, device, ws)
     if rank == 0 and not args.no_cpu:
-        result["cpu_baseline"] = cpu_baseline(g, sources)
+        base, cert = cpu_leg(g, timed_rows, config_rows, graphgen)
+        result["cpu_baseline"] = base
+        result["status_after_timing"] = cert["timed"]
+        if "per_config" in result:
+            for cfg, flag in cert["configs"].items():
+                result["per_config"][cfg]["parity"] = flag
     if rank == 0:
         print(json.dumps(result), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
+
+
+def per_level_table(counts, per_bytes, stats, peak):
+    """One search's levels: direction, advance, sizes, algorithmic bytes, the
+    time from this level's start to the next one's (device stamps; the last
+    level up to the end of its work), and the fraction of peak."""
+    rows = []
+    for i, (c, b) in enumerate(zip(counts, per_bytes)):
+        t0 = stats[i]["t_start_ns"]
+        t1 = stats[i + 1]["t_start_ns"] if i + 1 < len(stats) else stats[i]["t_work_ns"]
+        us = max(t1 - t0, 1) / 1e3
+        busy = max(stats[i]["t_work_ns"] - t0, 0) / 1e3
+        gbs = b / (us * 1e-6) / 1e9
+        rows.append({"level": c["level"], "dir": "push" if c["direction"] == DIR_PUSH else "pull",
+                     "advance": {0: "-", 1: "binned", 2: "merge_path", 3: "single_cta"}.get(
+                         c["advance"], str(c["advance"])),
+                     "F": c["F"], "m_F": c["mF"], "U": c["U"], "N": c["N"], "c": c["c"],
+                     "bytes": int(b), "us": round(us, 2), "busy_us": round(busy, 2),
+                     "gbs": round(gbs, 1), "frac": round(gbs / peak, 4)})
+    return rows
 
 
 def read_traffic_summary(cfg: int):
@@ -432,11 +559,159 @@ def read_traffic_summary(cfg: int):
         return None
 
 
+def time_search(torch, bfs, s, dist, parent, stream, warm=3, reps=10):
+    """Mean device time of bfs_csr_run (init + level loop) over `reps` runs
+    after `warm` untimed ones (the Day 38 protocol), CUDA events."""
+    for _ in range(warm):
+        bfs.run(s, dist, parent, stream=stream)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        bfs.run(s, dist, parent, stream=stream)
+    e1.record(stream)
+    levels = bfs.sync(stream)
+    return e0.elapsed_time(e1) / reps, levels
+
+
+def per_config(torch, fbc, graphgen, device, peak, rows_out, keep_rows=True):
+    """Configs 1-4: per source, the mean of 10 timed bfs_csr_run (after 3
+    warm-ups); GTEPS as the median over sources and the aggregate (sum of
+    edges over sum of times); the fraction of the HBM roofline of the whole
+    run (init + levels, scope-table bytes) over its time. Each source's
+    outputs are kept for the oracle's certification in the CPU leg."""
+    out = {}
+    stream = torch.cuda.current_stream(device)
+    for cfg in (1, 2, 3, 4):
+        g = graphgen.config(cfg)
+        row_ptr, col, row64, deg = graph_tensors(torch, g, device)
+        R = 8 if g.row_ptr_64 else 4
+        srcs = [int(s) for s in g.sources]
+        bfs = fbc.BfsCsr(row_ptr, col, symmetric=True)
+        dist = torch.empty(g.n, dtype=torch.int32, device=device)
+        parent = torch.empty_like(dist)
+        soe = torch.repeat_interleave(torch.arange(g.n, device=device, dtype=torch.int32), deg)
+        gteps, times, edges_l, bytes_l, levels_l = [], [], [], [], []
+        dist_rows, par_rows, lev_rows = [], [], []
+        overhead = None
+        for s in srcs:
+            ms, levels = time_search(torch, bfs, s, dist, parent, stream)
+            reached_mask = dist >= 0
+            reached = int(reached_mask.sum().item())
+            edges = int(deg[reached_mask].sum().item())
+            stats = bfs.level_stats()
+            counts = level_counts(torch, row64, col, deg, soe, dist, stats)
+            sb, _, _ = search_bytes(counts, g.n, R, reached)
+            b_run = sb + init_bytes_survey(g.n)
+            gteps.append(edges / (ms * 1e-3) / 1e9)
+            times.append(ms)
+            edges_l.append(edges)
+            bytes_l.append(b_run)
+            levels_l.append(levels)
+            if cfg == 4:
+                busy_ns = sum(max(x["t_work_ns"] - x["t_start_ns"], 0) for x in stats)
+                overhead = {"t_run_us": round(ms * 1e3, 1), "levels": levels,
+                            "busy_us": round(busy_ns / 1e3, 1),
+                            "overhead_us_per_level": round((ms * 1e3 - busy_ns / 1e3) / levels, 3),
+                            "definition": "(t_run - sum over levels of (last CTA's work end - "
+                                          "level start)) / levels, persistent loop"}
+            if keep_rows:
+                dist_rows.append(dist.cpu().numpy())
+                par_rows.append(parent.cpu().numpy())
+                lev_rows.append(levels)
+        bfs.close()
+        del soe
+        torch.cuda.empty_cache()
+        agg = sum(edges_l) / (sum(times) * 1e-3) / 1e9
+        frac = sum(bytes_l) / (sum(times) * 1e-3) / 1e9 / peak
+        entry = {"workload": WORKLOADS[cfg], "n": g.n, "nnz": g.nnz, "sources": len(srcs),
+                 "gteps_median": round(statistics.median(gteps), 4),
+                 "gteps_aggregate": round(agg, 4),
+                 "ms_per_search_median": round(statistics.median(times), 4),
+                 "levels_median": statistics.median(levels_l),
+                 "roofline_frac": round(frac, 4),
+                 "timing": "bfs_csr_run (init + levels), CUDA events, 3 warm-ups + 10 timed "
+                           "per source, one search at a time on the whole GPU",
+                 "parity": "not certified (--no-cpu)"}
+        if overhead is not None:
+            entry["per_level_overhead"] = overhead
+        out[str(cfg)] = entry
+        if keep_rows:
+            rows_out[str(cfg)] = (g, srcs, dist_rows, par_rows, lev_rows)
+    return out
+
+
+ABLATION = [
+    ("auto_dir+auto_adv", dict()),
+    ("push_only+auto_adv", dict(direction=1)),
+    ("pull_only", dict(direction=2)),
+    ("push_only+binned", dict(direction=1, advance=1)),
+    ("push_only+merge_path", dict(direction=1, advance=2)),
+    ("auto_dir+binned", dict(advance=1)),
+    ("auto_dir+merge_path", dict(advance=2)),
+]
+
+
+def ablation(torch, fbc, graphgen, device, cases, nsrc=16, reps=3):
+    """Direction (push only, pull only, the automatic rule) and push advance
+    (degree-binned, merge path, the automatic hybrid that takes the merge path
+    from a 4,096-vertex frontier or an 8,192-degree hub) on the first 16
+    sources of each config: one search at a time (lanes = 1), GTEPS of a
+    bfs_csr_run_batch over the sources, median of `reps` timed batches after
+    one warm-up. Each variant's distances are compared with the automatic
+    variant's (the option matrix of the tests checks every variant against
+    the oracle)."""
+    out = {}
+    stream = torch.cuda.current_stream(device)
+    for cfg, g in cases:
+        if g is None:
+            g = graphgen.config(cfg)
+        row_ptr, col, row64, deg = graph_tensors(torch, g, device)
+        srcs = [int(s) for s in g.sources[:nsrc]]
+        k = len(srcs)
+        dist = torch.empty((k, g.n), dtype=torch.int32, device=device)
+        ref = None
+        edges = None
+        res = {}
+        for name, over in ABLATION:
+            bfs = fbc.BfsCsr(row_ptr, col, symmetric=True, options=fbc.default_options(**over))
+            bfs.run_batch(srcs, dist, stream=stream)
+            if edges is None:
+                edges = sum(int(deg[dist[i] >= 0].sum().item()) for i in range(k))
+            ts = []
+            for _ in range(reps):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                bfs.run_batch(srcs, dist, stream=stream)
+                e1.record(stream)
+                torch.cuda.synchronize(device)
+                ts.append(e0.elapsed_time(e1))
+            bfs.close()
+            ms = statistics.median(ts)
+            if ref is None:
+                ref = dist.clone()
+                same = True
+            else:
+                same = bool(torch.equal(dist, ref))
+            res[name] = {"gteps": round(edges / (ms * 1e-3) / 1e9, 2),
+                         "ms_per_search": round(ms / k, 4), "same_dist_as_auto": same}
+        auto = res["auto_dir+auto_adv"]["gteps"]
+        for name in res:
+            res[name]["vs_auto"] = round(res[name]["gteps"] / auto, 3) if auto else None
+        out[str(cfg)] = {"sources": k, "variants": res}
+        del dist, ref, row_ptr, col, row64, deg
+        torch.cuda.empty_cache()
+    return out
+
+
 def per_level_overhead(torch, fbc, graphgen, device):
-    """Time per level on graphs made of narrow levels: the 2048x2048 grid from
-    its corner, and a 10,000-vertex path (one vertex per level), in the
+    """Per-level cost on graphs made of narrow levels: the 2048x2048 grid from
+    its corner and a 10,000-vertex path (one vertex per level), in the
     persistent loop and in the host loop (one launch + one device->host read
-    per level, the structure the Day 38 page measures)."""
+    per level, the structure the Day 38 page measures). `*_us` is t_run per
+    level; `*_sync_us` is (t_run - sum of level busy times) / levels, busy =
+    last CTA's work end - level start from the level records."""
     out = {}
     cases = [("grid_2048", graphgen.config(4)), ("path_10000", graphgen.path_graph(10000))]
     for name, g in cases:
@@ -451,15 +726,20 @@ def per_level_overhead(torch, fbc, graphgen, device):
             b.run(s, dist)
             levels = b.sync()
             reps = 3 if loop == fbc.BFS_CSR_LOOP_PERSISTENT else 1
-            times = []
+            best, best_busy = None, None
             for _ in range(reps):
                 torch.cuda.synchronize(device)
                 t = time.perf_counter()
                 b.run(s, dist)
                 b.sync()
-                times.append(time.perf_counter() - t)
+                el = time.perf_counter() - t
+                stats = b.level_stats()
+                bz = sum(max(x["t_work_ns"] - x["t_start_ns"], 0) for x in stats) * 1e-9
+                if best is None or el < best:
+                    best, best_busy = el, bz
             b.close()
-            row[mode] = round(min(times) * 1e6 / levels, 3)
+            row[mode] = round(best * 1e6 / levels, 3)
+            row[mode + "_sync"] = round((best - best_busy) * 1e6 / levels, 3)
             row["levels"] = levels
         out[name] = row
     return out
@@ -497,24 +777,73 @@ def run_e2e(torch, fbc, g, sources, args, device, ws):
             "api": "bfs_csr_create_host / bfs_csr_run_host_batch"}
 
 
-def cpu_baseline(g, sources, budget_s: float = 20.0):
-    """The oracle (sequential FIFO BFS in C, one host thread) on a bounded
-    sample of the same workload: sources in order until ~budget_s seconds."""
+# ------------------------------------------------------------------ CPU leg
+
+def cpu_leg(g, timed_rows, config_rows, graphgen, budget_s: float = 20.0):
+    """The oracle on the host, after every GPU measurement.
+
+    (1) Baseline: the sequential FIFO BFS (C, one host thread) on a bounded
+    sample of the timed workload, sources in order until ~budget_s seconds.
+    (2) Certification of the GPU outputs: every row of the last timed step
+    (and every per-config row) -- dist equal element by element to the
+    oracle's where the baseline computed it, else accepted by the oracle's
+    exact distance certificate; parent accepted by the oracle's tree check;
+    the level count equal to max(dist) + 1. The checks run on several host
+    threads at once (the oracle's ctypes calls release the GIL)."""
+    from concurrent.futures import ThreadPoolExecutor
+
     import oracle
     deg = np.diff(g.row_ptr.astype(np.int64))
+    known = {}
     done, edges, elapsed = [], 0, 0.0
-    for s in sources:
+    srcs = timed_rows[0] if timed_rows is not None else [int(s) for s in g.sources]
+    for s in srcs:
         t = time.perf_counter()
         d, _, _ = oracle.bfs(g.row_ptr, g.col, s, want_parent=True)
         elapsed += time.perf_counter() - t
         edges += int(deg[d >= 0].sum())
         done.append(s)
+        known[s] = d
         if elapsed > budget_s:
             break
-    return {"value": round(edges / elapsed / 1e9, 4), "unit": "GTEPS", "cores": 1,
+    cores = host_cores()
+    base = {"value": round(edges / elapsed / 1e9, 4), "unit": "GTEPS", "cores": 1,
+            "host_cores": cores["online"], "host_cores_affinity": cores["affinity"],
             "kind": "oracle",
-            "sample": "%d of %d sources of the timed workload, %.1f s" % (len(done), len(sources),
-                                                                          elapsed)}
+            "sample": "%d of %d sources of the timed workload (a sample), %.1f s on one thread"
+                      % (len(done), len(srcs), elapsed)}
+
+    def certify(graph, s, d, p, lev, want=None):
+        if want is not None:
+            ok_d = bool(np.array_equal(d, want))
+        else:
+            ok_d = oracle.check_dist(graph.row_ptr, graph.col, s, d)[0] == 0
+        ok_p = oracle.check_parent(graph.row_ptr, graph.col, s, d, p)[0] == 0
+        return ok_d and ok_p and int(lev) == int(d.max()) + 1, want is not None
+
+    workers = max(1, min(16, os.cpu_count() or 1))
+    cert = {"timed": "not certified", "configs": {}}
+    with ThreadPoolExecutor(max_workers=workers) as ex:
+        if timed_rows is not None:
+            srcs_t, dist_t, par_t, lev_t = timed_rows
+            res = list(ex.map(lambda i: certify(g, srcs_t[i], dist_t[i], par_t[i], lev_t[i],
+                                                known.get(srcs_t[i])), range(len(srcs_t))))
+            good = sum(1 for ok, _ in res if ok)
+            eq = sum(1 for _, e in res if e)
+            cert["timed"] = ("oracle-certified: %d/%d rows of the last timed step (%d equal "
+                             "element by element to the oracle's dist, the rest by its exact "
+                             "distance certificate; every parent row tree-checked)"
+                             % (good, len(res), eq)) if good == len(res) else \
+                ("error: %d of %d rows of the last timed step failed the oracle's checks"
+                 % (len(res) - good, len(res)))
+        for cfg, (gc, s_c, d_c, p_c, l_c) in config_rows.items():
+            res = list(ex.map(lambda i: certify(gc, s_c[i], d_c[i], p_c[i], l_c[i]),
+                              range(len(s_c))))
+            good = sum(1 for ok, _ in res if ok)
+            cert["configs"][cfg] = ("oracle-certified %d/%d sources" % (good, len(res))
+                                    if good == len(res) else
+                                    "error: %d/%d sources failed" % (len(res) - good, len(res)))
+    return base, cert
 
 
 # ------------------------------------------------------------------ reference arm
@@ -540,6 +869,7 @@ def run_reference(args):
         elapsed += time.perf_counter() - t
         edges += int(deg[d >= 0].sum())
     value = edges / elapsed / 1e9
+    cores = host_cores()
     line = {"metric": METRIC, "value": round(value, 4), "unit": "GTEPS", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(elapsed * 1e3 / args.steps, 3), "higher_is_better": True,
@@ -548,6 +878,8 @@ def run_reference(args):
             "config": {"workload": WORKLOADS[args.config], "n": g.n, "nnz": g.nnz,
                        "sources_per_step": 1},
             "cpu_baseline": {"value": round(value, 4), "unit": "GTEPS", "cores": 1,
+                             "host_cores": cores["online"],
+                             "host_cores_affinity": cores["affinity"],
                              "kind": "oracle",
                              "sample": "one source per step, %d steps" % args.steps},
             "e2e": {"value": round(value, 4), "unit": "GTEPS", "h2d_bytes_per_step": 0,
@@ -565,6 +897,10 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-overhead", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-config GTEPS / roofline / parity of configs 1-4")
+    ap.add_argument("--no-ablation", action="store_true",
+                    help="skip the direction / advance ablation")
     ap.add_argument("--lanes", type=int, default=2,
                     help="searches bfs_csr_run_batch keeps in flight (1..8)")
     ap.add_argument("--sources", type=int, default=0,

@@ -38,13 +38,14 @@ BFS_CSR_DIR_AUTO, BFS_CSR_DIR_PUSH, BFS_CSR_DIR_PULL = 0, 1, 2
 BFS_CSR_ADV_AUTO, BFS_CSR_ADV_BINNED, BFS_CSR_ADV_MERGE_PATH, BFS_CSR_ADV_SINGLE_CTA = 0, 1, 2, 3
 BFS_CSR_DISC_BITMAP, BFS_CSR_DISC_CAS = 0, 1
 BFS_CSR_LOOP_PERSISTENT, BFS_CSR_LOOP_HOST = 0, 1
+BFS_CSR_WALK_THREAD, BFS_CSR_WALK_WARP, BFS_CSR_WALK_BINNED, BFS_CSR_WALK_EDGE = 0, 1, 2, 3
 
 EXPORTED = [
     "bfs_csr_default_options", "bfs_csr_workspace_bytes", "bfs_csr_create", "bfs_csr_run",
     "bfs_csr_run_init", "bfs_csr_run_levels",
     "bfs_csr_sync", "bfs_csr_level_stats", "bfs_csr_create_host", "bfs_csr_run_host",
     "bfs_csr_run_host_batch", "bfs_csr_destroy", "bfs_csr_status_string", "bfs_csr_last_cuda_error",
-    "bfs_csr_run_noalloc", "bfs_csr_run_batch",
+    "bfs_csr_run_noalloc", "bfs_csr_run_batch", "bfs_csr_walk",
 ]
 BFS_CSR_NOALLOC_MAX_VERTICES = 1048576
 
@@ -84,6 +85,7 @@ class bfs_csr_level_stat(ctypes.Structure):
         ("unvisited", ctypes.c_int64),
         ("max_degree", ctypes.c_int64),
         ("t_start_ns", ctypes.c_int64),
+        ("t_work_ns", ctypes.c_int64),
     ]
 
 
@@ -110,6 +112,7 @@ _sig = {
     "bfs_csr_run_noalloc": ([_i64, _i64, _vp, _vp, _i32, _i64, _vp, _vp, _vp,
                              ctypes.POINTER(ctypes.c_int32), _opt_p, _vp], _i32),
     "bfs_csr_run_batch": ([_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp], _i32),
+    "bfs_csr_walk": ([_vp, _vp, _i32, _i32, _i32, _vp, _vp], _i32),
 }
 for _name, (_args, _res) in _sig.items():
     _f = getattr(_lib, _name)
@@ -239,6 +242,19 @@ class BfsCsr:
                                    _stream_ptr(stream))
         _check(status, "bfs_csr_run_batch", self.handle)
 
+    def walk(self, frontier, repeats: int, mapping: int, out, stream=None) -> None:
+        """Enqueue the isolated neighbour walk of `frontier` (int32 CUDA
+        tensor of vertex ids): out[i] (int32 or uint32 CUDA tensor, same
+        length) gets the wrapping 32-bit sum over r < repeats and the entries
+        e of frontier[i]'s row of col[e] XOR r."""
+        size = int(frontier.numel())
+        if out.numel() != size or not (frontier.is_contiguous() and out.is_contiguous()):
+            raise ValueError("frontier and out must be contiguous and of the same length")
+        status = bfs_csr_walk(self.handle, frontier.data_ptr() if size else None, size,
+                              int(repeats), int(mapping), out.data_ptr() if size else None,
+                              _stream_ptr(stream))
+        _check(status, "bfs_csr_walk", self.handle)
+
     def search(self, source: int, want_parent: bool = True, stream=None):
         """Run one search and wait: returns (dist, parent or None, num_levels)."""
         import torch
@@ -261,7 +277,7 @@ class BfsCsr:
             out.append({"level": s.level, "direction": s.direction, "advance": s.advance,
                         "frontier": s.frontier, "frontier_edges": s.frontier_edges,
                         "unvisited": s.unvisited, "max_degree": s.max_degree,
-                        "t_start_ns": s.t_start_ns})
+                        "t_start_ns": s.t_start_ns, "t_work_ns": s.t_work_ns})
         return out
 
     def close(self) -> None:

@@ -1294,6 +1294,7 @@ __device__ void solo_levels(const Params<RowT>& p, int k, int qn, RowT qm, long 
             st.unvisited = Uj;
             st.max_degree = (long long)mdj;
             st.t_start_ns = (long long)t0;
+            st.t_work_ns = (long long)global_timer_ns();
             p.stats[j] = st;
         }
         const long long Un = Uj - Fn;   // unvisited at level j + 1's start
@@ -1344,6 +1345,8 @@ __device__ void solo_levels(const Params<RowT>& p, int k, int qn, RowT qm, long 
                 sa->work_next = 0u;
                 sn->work_next = 0u;
                 p.ctl->solo_resume = jn;
+                if (jn < p.stats_cap)
+                    p.stats[jn].t_work_ns = 0;
             }
             stage_flush(p, sm, ss, &p.ctl->slot[jn & 3], jn & 1);
             return;
@@ -1527,6 +1530,7 @@ __global__ void __launch_bounds__(512, 2) level_kernel(Params<RowT> p)
                     st.unvisited = uprev - F;
                     st.max_degree = (long long)maxdeg;
                     st.t_start_ns = (long long)t_end;
+                    st.t_work_ns = (long long)t_end;
                     p.stats[k] = st;
                 }
                 p.ctl->num_levels = nl;
@@ -1623,18 +1627,25 @@ __global__ void __launch_bounds__(512, 2) level_kernel(Params<RowT> p)
             else
                 push_binned(p, k, qn, qm, sm, ss, nxt, t, pre);
         }
+        // The level's record. Every CTA stamps the end of its share of the
+        // work (the latest stamp wins); the next level's stamp is cleared
+        // here, before the barrier after which CTAs write it.
+        if (threadIdx.x == 0 && k < p.stats_cap)
+            atomicMax(reinterpret_cast<unsigned long long*>(&p.stats[k].t_work_ns),
+                      global_timer_ns());
         if (leader && k < p.stats_cap) {
-            bfs_csr_level_stat st;
-            st.level = k;
-            st.direction = dir;
-            st.advance = adv;
-            st.reserved = 0;
-            st.frontier = F;
-            st.frontier_edges = mF;
-            st.unvisited = U;
-            st.max_degree = (long long)maxdeg;
-            st.t_start_ns = (long long)t_level;
-            p.stats[k] = st;
+            bfs_csr_level_stat* st = &p.stats[k];
+            st->level = k;
+            st->direction = dir;
+            st->advance = adv;
+            st->reserved = 0;
+            st->frontier = F;
+            st->frontier_edges = mF;
+            st->unvisited = U;
+            st->max_degree = (long long)maxdeg;
+            st->t_start_ns = (long long)t_level;
+            if (k + 1 < p.stats_cap)
+                p.stats[k + 1].t_work_ns = 0;
         }
         publish_tally<RowT>(t, nxt, ss);
         if (!grid_barrier(p, target)) break;
@@ -1743,6 +1754,8 @@ __global__ void init_kernel(Params<RowT> p, const uint32_t* __restrict__ dead, i
             c->slot[s].adv = 0;
             c->slot[s].work_next = 0u;
         }
+        if (p.stats != nullptr && p.stats_cap > 0)
+            p.stats[0].t_work_ns = 0;
         c->slot[0].found = 1ull;
         c->slot[0].fedges = (unsigned long long)deg;
         c->slot[0].maxdeg = (unsigned long long)deg;

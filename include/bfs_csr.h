@@ -246,6 +246,37 @@ int bfs_csr_run_host_batch(bfs_csr_handle h, int32_t num_sources, const int64_t 
                            int32_t *h_dist, int32_t *h_parent, int32_t *h_num_levels,
                            void *stream);
 
+/*
+ * The isolated neighbour walk of one frontier, the measurement of "100 Days
+ * of GPU, Day 38: Graph traversal on a GPU", section "Measuring the mapping
+ * without measuring the launch": the handle's CSR rows of the frontier's
+ * vertices are read `repeats` times with no claims, no frontier build and no
+ * distance writes, so that one level's mapping can be timed on its own. For
+ * slot i of d_frontier (device, frontier_size int32 vertex ids, 0 <=
+ * frontier_size <= n) with vertex u, d_out[i] (device, frontier_size uint32)
+ * receives
+ *     sum over r < repeats and over e in [row_ptr[u], row_ptr[u + 1]) of
+ *     (col[e] XOR r), modulo 2^32,
+ * the same value for every mapping (unsigned addition wraps and commutes),
+ * which a caller predicts exactly on the host. An entry outside [0, n)
+ * walks nothing (its slot gets 0).
+ * mapping: BFS_CSR_WALK_THREAD one thread per vertex, _WARP one warp per
+ * vertex (the page's two mappings), _BINNED thread / warp / CTA by degree
+ * with the handle's small_max_degree and cta_min_degree (the push levels'
+ * mapping), _EDGE edge-balanced over the prefix of the frontier's degrees
+ * (the merge path's mapping; the prefix is built first, on the device, in
+ * the handle's workspace). Asynchronous on `stream`; it uses the workspace
+ * of the handle's first lane, so it must not overlap a search on the same
+ * handle. BFS_CSR_EINVAL for a NULL pointer (with frontier_size > 0), a
+ * size outside [0, n], repeats < 0 or an unknown mapping.
+ */
+#define BFS_CSR_WALK_THREAD 0
+#define BFS_CSR_WALK_WARP 1
+#define BFS_CSR_WALK_BINNED 2
+#define BFS_CSR_WALK_EDGE 3
+int bfs_csr_walk(bfs_csr_handle h, const int32_t *d_frontier, int32_t frontier_size,
+                 int32_t repeats, int32_t mapping, uint32_t *d_out, void *stream);
+
 /* Release everything the library allocated for the handle. */
 int bfs_csr_destroy(bfs_csr_handle h);
 

@@ -62,7 +62,7 @@ int main(void) {
   F(bfs_csr_level_stat, level); F(bfs_csr_level_stat, direction); F(bfs_csr_level_stat, advance);
   F(bfs_csr_level_stat, frontier); F(bfs_csr_level_stat, frontier_edges);
   F(bfs_csr_level_stat, unvisited); F(bfs_csr_level_stat, max_degree);
-  F(bfs_csr_level_stat, t_start_ns);
+  F(bfs_csr_level_stat, t_start_ns); F(bfs_csr_level_stat, t_work_ns);
   return 0;
 }
 '''
@@ -84,7 +84,7 @@ def test_struct_layouts_match_header(fbc):
     for name, _ in fbc.bfs_csr_options._fields_:
         assert getattr(fbc.bfs_csr_options, name).offset == lay["bfs_csr_options." + name], name
     for name in ("level", "direction", "advance", "frontier", "frontier_edges", "unvisited",
-                 "max_degree", "t_start_ns"):
+                 "max_degree", "t_start_ns", "t_work_ns"):
         assert getattr(fbc.bfs_csr_level_stat, name).offset == lay["bfs_csr_level_stat." + name], name
 
 

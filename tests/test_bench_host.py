@@ -19,38 +19,65 @@ def test_busy_time_is_the_union_of_intervals():
     assert bench.busy_time([(0.0, 1.0), (1.0, 2.0)]) == 2.0            # touching
 
 
-def _model(g, dist, dirs):
+def _counts(g, dist, dirs):
     rp = torch.from_numpy(g.row_ptr.astype(np.int64))
     col = torch.from_numpy(g.col)
     deg = torch.diff(rp)
     src_of_edge = torch.repeat_interleave(torch.arange(g.n, dtype=torch.int32), deg)
-    stats = [{"direction": d} for d in dirs]
-    return bench.algorithmic_bytes(torch, rp, col, deg, src_of_edge,
-                                   torch.tensor(dist, dtype=torch.int32), stats, 4)
+    stats = [{"direction": d, "advance": 0} for d in dirs]
+    return bench.level_counts(torch, rp, col, deg, src_of_edge,
+                              torch.tensor(dist, dtype=torch.int32), stats)
 
 
-def test_byte_model_push_levels_by_hand():
-    # path 0-1-2 from 0, int32 row_ptr (R = 4): per push level
-    # (4+2R)|Q| + 4 m_F + 4 m_F + 2R|N| + 8|N| + 4|N| + (4+2R)|N'|
+def test_byte_models_push_levels_by_hand():
+    # path 0-1-2 from 0, int32 row_ptr (R = 4)
     g = graphgen.path_graph(3)
-    total, per_level = _model(g, [0, 1, 2], [bench.DIR_PUSH] * 3)
-    assert per_level == [12 + 4 + 4 + 8 + 8 + 4 + 12,    # F = {0}, m_F = 1, N = {1}
-                         12 + 8 + 8 + 8 + 8 + 4 + 12,    # F = {1}, m_F = 2, N = {2}
-                         12 + 4 + 4]                      # F = {2}, m_F = 1, N = {}
-    assert total == sum(per_level)
+    counts = _counts(g, [0, 1, 2], [bench.DIR_PUSH] * 3)
+    assert [(c["F"], c["mF"], c["N"]) for c in counts] == [(1, 1, 1), (1, 2, 1), (1, 1, 0)]
+    # scope table, push: 4|F| + 2R|F| + 4 m_F (col) + 4 m_F (probe) + 8|N| + 4|N| + |N|/8
+    assert [bench.survey_bytes(c, 3, 4) for c in counts] == [4 + 8 + 8 + 8 + 4,
+                                                             4 + 8 + 16 + 8 + 4,
+                                                             4 + 8 + 8]
+    # the kernel: queue entries (4 + 2R) per vertex with edges, row offsets of
+    # every winner 2R, queue entries written (4 + 2R)
+    s_tot, k_tot, per = bench.search_bytes(counts, 3, 4, reached=3)
+    assert per == [32, 40, 20] and s_tot == 92
+    assert k_tot == (12 + 4 + 4 + 8 + 8 + 4 + 12) + (12 + 8 + 8 + 8 + 8 + 4 + 12) + (12 + 4 + 4)
 
 
-def test_byte_model_pull_level_and_switches_by_hand():
+def test_byte_models_pull_level_and_switches_by_hand():
     # star 0-{1,2,3} from leaf 1: push, pull, push; plus one isolated vertex 4
     g = graphgen.from_edges(5, [0, 0, 0], [1, 2, 3])
-    total, per_level = _model(g, [1, 0, 2, 2, -1],
-                              [bench.DIR_PUSH, bench.DIR_PULL, bench.DIR_PUSH])
-    words = 1
-    push0 = 12 + 4 + 4 + 8 + 8 + 4 + 12                  # F = {1}, N = {0}
-    to_bitmap = 4 * words + 8 * 1                         # queue {0} -> bitmap
-    # pull over U' = {2, 3}: each scans one entry (its only neighbour, 0, is in F)
-    pull1 = 4 * words + 8 * 2 + 4 * 2 + 4 * 2 + 8 * 2 + 4 * words + 4 * 1
-    to_queue = 4 * words + 8 * 2 + 12 * 2                 # bitmap {2, 3} -> queue
-    push2 = 12 * 2 + 4 * 2 + 4 * 2                        # F = {2, 3}, N = {}
-    assert per_level == [push0, to_bitmap + pull1, to_queue + push2]
-    assert total == sum(per_level) + 4 * 1                # dist of the unreached vertex 4
+    counts = _counts(g, [1, 0, 2, 2, -1], [bench.DIR_PUSH, bench.DIR_PULL, bench.DIR_PUSH])
+    # level 1 pulls over U = {2, 3} (vertex 4 has no edges): each finds its
+    # only neighbour 0 after one entry
+    assert (counts[1]["U"], counts[1]["c"], counts[1]["N"], counts[1]["tw"]) == (2, 2, 2, 1)
+    n, words = 5, 1
+    push0 = 4 + 8 + 8 + 8 + 4                              # F = {1}, m_F = 1, N = {0}
+    pull1 = n // 8 + 8 * 2 + 8 * 2 + 8 * 2 + n // 8       # 2R|U| + 8c + 8|N|
+    push2 = 4 * 2 + 8 * 2 + 8 * 2                          # F = {2, 3}, m_F = 2, N = {}
+    s_tot, k_tot, per = bench.search_bytes(counts, n, 4, reached=4)
+    assert per == [push0, pull1, push2] and s_tot == sum(per)
+    k_push0 = 12 + 4 + 4 + 8 + 8 + 4 + 12
+    to_bitmap = 4 * words + 8 * 1                          # queue {0} -> bitmap
+    k_pull1 = 4 * words + 8 * 2 + 4 * 2 + 4 * 2 + 8 * 2 + 4 * words + 4 * 1
+    to_queue = 4 * words + 8 * 2 + 12 * 2                  # bitmap {2, 3} -> queue
+    k_push2 = 12 * 2 + 4 * 2 + 4 * 2
+    assert k_tot == k_push0 + to_bitmap + k_pull1 + to_queue + k_push2 + 4 * 1
+
+
+def test_pull_scan_counts_stop_at_the_first_frontier_neighbour():
+    # edges 0-3, 3-5, 5-1, 5-2, 5-4, 1-6, 2-6; from 0 the distances are
+    # 3:1, 5:2, {1, 2, 4}:3, 6:4. Vertex 5's row is [1, 2, 3, 4] and only 3
+    # is at distance 1, so a bottom-up scan of 5 reads three entries.
+    g = graphgen.from_edges(7, [0, 3, 5, 5, 5, 1, 2], [3, 5, 1, 2, 4, 6, 6])
+    dist = [0, 3, 3, 1, 3, 2, 4]
+    counts = _counts(g, dist, [bench.DIR_PUSH, bench.DIR_PULL, bench.DIR_PULL, bench.DIR_PULL,
+                               bench.DIR_PUSH])
+    assert g.col[g.row_ptr[5]:g.row_ptr[6]].tolist() == [1, 2, 3, 4]
+    # level 1: U = {1, 2, 4, 5, 6}; 5 is found at its 3rd entry; 1 (row [5, 6]),
+    # 2 (row [5, 6]), 4 (row [5]) and 6 (row [1, 2]) are scanned whole
+    assert counts[1]["U"] == 5 and counts[1]["N"] == 1
+    assert counts[1]["c"] == 3 + 2 + 2 + 1 + 2
+    # level 2: U = {1, 2, 4, 6}; 1, 2, 4 find 5 at their first entry; 6 whole row
+    assert counts[2]["c"] == 1 + 1 + 1 + 2
