@@ -500,6 +500,8 @@ def run_ours(args):
         result["ablation"] = ablation(torch, fbc, graphgen, device, cases)
     if rank == 0 and not args.no_overhead:
         result["per_level_overhead_us"] = per_level_overhead(torch, fbc, graphgen, device)
+    if rank == 0 and not args.no_walk:
+        result["walk"] = walk_section(torch, fbc, graphgen, device)
     if not args.no_e2e:
         result["e2e"] = run_e2e(torch, fbc, g, sources, args, device, ws)
     if rank == 0 and not args.no_cpu:
@@ -705,6 +707,92 @@ def ablation(torch, fbc, graphgen, device, cases, nsrc=16, reps=3):
     return out
 
 
+def lane_slots(degrees):
+    """Lane slots a level's neighbour walk issues ("100 Days of GPU, Day 38",
+    the level table): with one thread per vertex each warp of 32 consecutive
+    frontier entries runs as long as its longest row, so it issues 32 times
+    its largest degree; with one warp per vertex each vertex takes
+    ceil(degree / 32) passes of 32 lanes."""
+    d = np.asarray(degrees, dtype=np.int64)
+    warps = (d.size + 31) // 32
+    pad = np.zeros(warps * 32, dtype=np.int64)
+    pad[:d.size] = d
+    thread = int(32 * pad.reshape(warps, 32).max(axis=1).sum()) if warps else 0
+    warp = int(32 * ((d + 31) // 32).sum())
+    return {"warps": int(warps), "thread": thread, "warp": warp, "edges": int(d.sum()),
+            "max_degree": int(d.max()) if d.size else 0,
+            "useful_thread": round(float(d.sum()) / thread, 4) if thread else None}
+
+
+WALK_MAPPINGS = ("thread", "warp", "binned", "edge")
+
+
+def walk_section(torch, fbc, graphgen, device, repeats=64, min_edges=1000):
+    """The isolated neighbour walk of single levels (Day 38, "Measuring the
+    mapping without measuring the launch") on the 3,485-vertex power-law
+    graph from its most eccentric source (most levels, smallest id on ties;
+    found by a GPU search from every vertex of nonzero degree): for every
+    level with at least 1,000 edges, the frontier (vertex order) walked 64
+    times by each mapping, 3 warm-ups + 10 timed launches (CUDA events, mean),
+    the graph-derived lane slots, and the pages' T4 figures as context. The
+    four mappings' checksums are compared with each other here; the tests
+    compare them with the oracle's."""
+    g = graphgen.config(1)
+    row_ptr, col, row64, deg = graph_tensors(torch, g, device)
+    bfs = fbc.BfsCsr(row_ptr, col, symmetric=True)
+    dist = torch.empty(g.n, dtype=torch.int32, device=device)
+    nl = torch.empty(1, dtype=torch.int32, device=device)
+    stream = torch.cuda.current_stream(device)
+    best, best_levels = None, -1
+    cand = torch.nonzero(deg > 0).squeeze(1).tolist()
+    lev = torch.empty(len(cand), dtype=torch.int32, device=device)
+    for i, s in enumerate(cand):
+        bfs.run(s, dist, None, lev[i:i + 1], stream=stream)
+    levels_all = lev.cpu().tolist()
+    for s, L in zip(cand, levels_all):
+        if L > best_levels:
+            best, best_levels = s, L
+    bfs.run(best, dist, None, nl, stream=stream)
+    bfs.sync(stream)
+    d_h = dist.cpu().numpy()
+    deg_h = np.diff(g.row_ptr.astype(np.int64))
+    rows, table = [], []
+    for k in range(best_levels):
+        frontier = np.nonzero(d_h == k)[0].astype(np.int32)
+        slots = lane_slots(deg_h[frontier])
+        table.append(dict(level=k, frontier=int(frontier.size), **slots))
+        if slots["edges"] < min_edges:
+            continue
+        fr = torch.from_numpy(frontier).to(device)
+        outs, ms = [], {}
+        for m, name in enumerate(WALK_MAPPINGS):
+            out = torch.empty(frontier.size, dtype=torch.int32, device=device)
+            for _ in range(3):
+                bfs.walk(fr, repeats, m, out, stream=stream)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(10):
+                bfs.walk(fr, repeats, m, out, stream=stream)
+            e1.record(stream)
+            torch.cuda.synchronize(device)
+            ms[name] = round(e0.elapsed_time(e1) / 10, 5)
+            outs.append(out.clone())
+        same = all(bool(torch.equal(outs[0], o)) for o in outs[1:])
+        rows.append({"level": k, "frontier": int(frontier.size), "edges": slots["edges"],
+                     "max_degree": slots["max_degree"], "ms": ms,
+                     "thread_over_warp": round(ms["thread"] / ms["warp"], 2),
+                     "lane_slots": {"thread": slots["thread"], "warp": slots["warp"]},
+                     "checksums_agree": same})
+    bfs.close()
+    return {"graph": WORKLOADS[1], "source": best, "levels": best_levels, "repeats": repeats,
+            "timing": "bfs_csr_walk, 3 warm-ups + 10 timed launches, CUDA events, mean",
+            "levels_timed": rows, "lane_slot_table": table,
+            "lane_slots_whole_search": {"thread": sum(t["thread"] for t in table),
+                                        "edges": sum(t["edges"] for t in table)},
+            "pages_context": PAGES_CONTEXT}
+
+
 def per_level_overhead(torch, fbc, graphgen, device):
     """Per-level cost on graphs made of narrow levels: the 2048x2048 grid from
     its corner and a 10,000-vertex path (one vertex per level), in the
@@ -901,6 +989,8 @@ def main():
                     help="skip the per-config GTEPS / roofline / parity of configs 1-4")
     ap.add_argument("--no-ablation", action="store_true",
                     help="skip the direction / advance ablation")
+    ap.add_argument("--no-walk", action="store_true",
+                    help="skip the isolated-level walk of the power-law graph")
     ap.add_argument("--lanes", type=int, default=2,
                     help="searches bfs_csr_run_batch keeps in flight (1..8)")
     ap.add_argument("--sources", type=int, default=0,

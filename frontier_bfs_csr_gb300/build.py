@@ -15,6 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 SOURCES = [os.path.join(HERE, "csrc", "bfs_csr.cu")]
 DEPENDS = SOURCES + [os.path.join(HERE, "csrc", "bfs_device.cuh"),
+                     os.path.join(HERE, "csrc", "walk_device.cuh"),
                      os.path.join(ROOT, "include", "bfs_csr.h")]
 LIB = os.path.join(HERE, "libbfs_csr.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -17,6 +17,7 @@
 
 #include "bfs_csr.h"
 #include "bfs_device.cuh"
+#include "walk_device.cuh"
 
 using fbc::Ctl;
 using fbc::Params;
@@ -835,6 +836,69 @@ int bfs_csr_run_batch(bfs_csr_handle h, int32_t num_sources, const int64_t* sour
     }
     h->last_status = first_bad;
     return first_bad;
+}
+
+}  // extern "C"
+
+namespace {
+
+template <typename RowT>
+int launch_walk(bfs_csr_t* h, const int32_t* frontier, int32_t size, int32_t repeats,
+                int32_t mapping, uint32_t* out, cudaStream_t s)
+{
+    const RowT* rp = static_cast<const RowT*>(h->row_ptr);
+    const int32_t n = (int32_t)h->n;
+    switch (mapping) {
+    case BFS_CSR_WALK_THREAD:
+        fbc::walk_thread_kernel<RowT><<<(size + 255) / 256, 256, 0, s>>>(rp, h->col, n, frontier,
+                                                                        size, repeats, out);
+        break;
+    case BFS_CSR_WALK_WARP: {
+        const int64_t threads = (int64_t)size * 32;
+        fbc::walk_warp_kernel<RowT><<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(
+            rp, h->col, n, frontier, size, repeats, out);
+        break;
+    }
+    case BFS_CSR_WALK_BINNED:
+        fbc::walk_binned_kernel<RowT><<<h->sm_count * 4, 256, 0, s>>>(
+            rp, h->col, n, frontier, size, repeats, h->opt.small_max_degree,
+            h->opt.cta_min_degree, out);
+        break;
+    default: {  // BFS_CSR_WALK_EDGE
+        // The frontier's degree prefix goes to the lane-0 queue offset
+        // arrays, which are consecutive in the workspace and hold at least
+        // n + 1 entries together.
+        RowT* offs = reinterpret_cast<RowT*>(h->ws + h->L.qoff0);
+        fbc::walk_prefix_kernel<RowT><<<1, 1024, 0, s>>>(rp, n, frontier, size, offs, out);
+        FBC_CUDA(h, cudaGetLastError());
+        fbc::walk_edge_kernel<RowT><<<h->sm_count * 8, 256, 0, s>>>(rp, h->col, n, frontier, size,
+                                                                    repeats, offs, out);
+        break;
+    }
+    }
+    FBC_CUDA(h, cudaGetLastError());
+    return BFS_CSR_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int bfs_csr_walk(bfs_csr_handle h, const int32_t* d_frontier, int32_t frontier_size,
+                 int32_t repeats, int32_t mapping, uint32_t* d_out, void* stream)
+{
+    if (h == nullptr || frontier_size < 0 || (int64_t)frontier_size > h->n || repeats < 0 ||
+        mapping < BFS_CSR_WALK_THREAD || mapping > BFS_CSR_WALK_EDGE)
+        return BFS_CSR_EINVAL;
+    if (frontier_size == 0)
+        return BFS_CSR_OK;
+    if (d_frontier == nullptr || d_out == nullptr)
+        return BFS_CSR_EINVAL;
+    cudaStream_t s = as_stream(stream);
+    return h->row_ptr_64 ? launch_walk<int64_t>(h, d_frontier, frontier_size, repeats, mapping,
+                                                d_out, s)
+                         : launch_walk<int32_t>(h, d_frontier, frontier_size, repeats, mapping,
+                                                d_out, s);
 }
 
 int bfs_csr_destroy(bfs_csr_handle h)

@@ -18,6 +18,9 @@ written at the top of ``bfs_oracle.c``. In short:
 * :func:`check_parent` -- BFS-tree validity (every parent is an in-neighbour
   one level up).
 * :func:`level_sizes` -- per-level frontier sizes and the walked-edge count.
+* :func:`walk_checksum` -- what the isolated neighbour walk of a frontier
+  returns per slot ("100 Days of GPU, Day 38", "Measuring the mapping
+  without measuring the launch").
 """
 from __future__ import annotations
 
@@ -66,6 +69,8 @@ def _load():
             lib.oracle_check_parent.restype = i32
             lib.oracle_level_sizes.argtypes = [i64, vp, i32, vp, vp, i64, vp, vp, vp]
             lib.oracle_level_sizes.restype = i32
+            lib.oracle_walk_checksum.argtypes = [i64, vp, i32, vp, vp, i64, i64, vp]
+            lib.oracle_walk_checksum.restype = i32
             _lib = lib
     return _lib
 
@@ -138,3 +143,17 @@ def level_sizes(row_ptr, dist, level_cap: int | None = None):
     if rc != OK:
         raise ValueError("oracle_level_sizes failed with code %d" % rc)
     return sizes[:level_cap], int(nl.value), int(reached.value), int(edges.value)
+
+
+def walk_checksum(row_ptr, col, frontier, repeats: int):
+    """Per frontier slot: the wrapping 32-bit sum over r < repeats and the
+    entries e of the slot's row of col[e] XOR r (uint32 array)."""
+    lib = _load()
+    n, rp, rp64, col = _csr(row_ptr, col)
+    fr = np.ascontiguousarray(frontier, dtype=np.int32)
+    out = np.zeros(fr.shape[0], dtype=np.uint32)
+    rc = lib.oracle_walk_checksum(n, _ptr(rp), rp64, _ptr(col), _ptr(fr), int(fr.shape[0]),
+                                  int(repeats), _ptr(out))
+    if rc != OK:
+        raise ValueError("oracle_walk_checksum failed with code %d" % rc)
+    return out

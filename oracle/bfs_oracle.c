@@ -55,6 +55,14 @@
  *    Day 38 level table). The sizes summing to the reached count is the
  *    gate that sees a vertex enqueued twice (Day 38, "Pitfalls").
  *
+ *  oracle_walk_checksum
+ *    What the isolated neighbour walk of one frontier must return ("100 Days
+ *    of GPU, Day 38", section "Measuring the mapping without measuring the
+ *    launch"): for each frontier slot, the neighbour ids of its vertex's
+ *    row XORed with the repeat counter r and summed over every repeat into
+ *    an unsigned 32-bit accumulator, where overflow wraps. Plain loops in
+ *    CSR order, repeat by repeat.
+ *
  * Every function takes the CSR as (n, row_ptr, row_ptr_64, col): row_ptr
  * holds n + 1 entries, int64 when row_ptr_64 is nonzero and int32
  * otherwise; col holds row_ptr[n] int32 vertex ids. Return codes: 0 means
@@ -283,5 +291,31 @@ int oracle_level_sizes(int64_t n, const void *row_ptr, int row_ptr_64,
         *reached = count;
     if (edges_walked != NULL)
         *edges_walked = edges;
+    return ORACLE_OK;
+}
+
+/* Walk checksum of every frontier slot; an entry outside [0, n) gets 0. */
+int oracle_walk_checksum(int64_t n, const void *row_ptr, int row_ptr_64,
+                         const int32_t *col, const int32_t *frontier,
+                         int64_t size, int64_t repeats, uint32_t *out)
+{
+    int64_t i, r, e;
+
+    if (n <= 0 || row_ptr == NULL || size < 0 || repeats < 0)
+        return ORACLE_EARG;
+    if (size > 0 && (frontier == NULL || out == NULL))
+        return ORACLE_EARG;
+    for (i = 0; i < size; ++i) {
+        const int32_t u = frontier[i];
+        uint32_t acc = 0u;
+        if (u >= 0 && u < n) {
+            const int64_t first = row_at(row_ptr, row_ptr_64, u);
+            const int64_t last = row_at(row_ptr, row_ptr_64, u + 1);
+            for (r = 0; r < repeats; ++r)
+                for (e = first; e < last; ++e)
+                    acc += (uint32_t)col[e] ^ (uint32_t)r;
+        }
+        out[i] = acc;
+    }
     return ORACLE_OK;
 }

@@ -81,3 +81,31 @@ def test_pull_scan_counts_stop_at_the_first_frontier_neighbour():
     assert counts[1]["c"] == 3 + 2 + 2 + 1 + 2
     # level 2: U = {1, 2, 4, 6}; 1, 2, 4 find 5 at their first entry; 6 whole row
     assert counts[2]["c"] == 1 + 1 + 1 + 2
+
+
+def test_lane_slots_against_the_day38_table(golden):
+    """Lane slots as the Day 38 table counts them. Its levels of at most 32
+    vertices run in one warp, so the thread mapping issues 32 x the largest
+    degree there; the degree lists below are consistent with the table and
+    text (level 4: ten vertices, 2,452 edges, degrees 1,255 and 1,012 and
+    eight of at most 43; level 6: 1,579 vertices, 3,851 edges, largest 33)
+    and reproduce its 40,160 thread and 2,656 warp slots for level 4 and
+    its 50,560 warp slots for level 6."""
+    t = golden("day38_level_table.json")
+    for f, e, md, w, slots in zip(t["frontier"], t["edges"], t["max_degree"], t["warps"],
+                                  t["lane_slots"]):
+        if f <= 32:
+            degrees = [md] + [1] * (f - 1)
+            r = bench.lane_slots(degrees)
+            assert r["warps"] == w == 1 and r["thread"] == slots == 32 * md
+    lvl4 = [1255, 1012, 43, 43, 43, 12, 11, 11, 11, 11]
+    assert len(lvl4) == 10 and sum(lvl4) == 2452
+    r = bench.lane_slots(lvl4)
+    assert (r["thread"], r["warp"], r["max_degree"]) == (40160, 2656, 1255)
+    lvl6 = [33] + [3] * 662 + [2] * 916
+    assert len(lvl6) == 1579 and sum(lvl6) == 3851
+    assert bench.lane_slots(lvl6)["warp"] == 50560
+    # hand counts: 33 entries of degree 1 and one of 40 take two thread warps
+    r = bench.lane_slots([1] * 33 + [40])
+    assert r["warps"] == 2 and r["thread"] == 32 * 1 + 32 * 40 and r["warp"] == 32 * 33 + 64
+    assert bench.lane_slots([])["thread"] == 0

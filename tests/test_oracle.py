@@ -332,6 +332,55 @@ def test_edges_walked_pinned_to_the_worked_examples(golden):
         assert oracle.level_sizes(g.row_ptr, d)[2:] == want
 
 
+def _xor_sum_by_bits(c: int, repeats: int) -> int:
+    """sum over r < repeats of (c XOR r), counted bit by bit: bit b of c ^ r is
+    set for every r whose bit b differs from c's, and among 0 .. R-1 the
+    number of r with bit b set is (R >> (b+1)) << b plus the overhang of the
+    last partial period. Independent of the oracle's loop."""
+    total = 0
+    for b in range(40):
+        period = 1 << (b + 1)
+        ones = (repeats // period) * (1 << b) + max(0, repeats % period - (1 << b))
+        n_set = repeats - ones if (c >> b) & 1 else ones
+        total += n_set << b
+    return total
+
+
+def test_walk_checksum_pins(golden):
+    """The walk checksum against values fixed without the oracle's loop.
+
+    One repeat (r = 0) is the plain sum of the neighbour ids: on the ch. 22
+    six-vertex graph the rows [1 2] [2 3] [3 4] [4 5] [5] [] sum to 3, 5, 7,
+    9, 5, 0. For a power-of-two repeat count P, XOR with r < P permutes the
+    low bits, so each entry c contributes P * (c with its low log2 P bits
+    cleared) + P (P - 1) / 2; the page's 64 repeats fall under this. Other
+    counts are checked bit by bit; the sum wraps modulo 2^32, and an id
+    outside [0, n) walks nothing."""
+    gx = golden("six_vertex_directed.json")
+    rp, col = np.array(gx["row_ptr"]), np.array(gx["col"])
+    assert oracle.walk_checksum(rp, col, [0, 1, 2, 3, 4, 5], 1).tolist() == [3, 5, 7, 9, 5, 0]
+    assert oracle.walk_checksum(rp, col, [0, 5, 0], 0).tolist() == [0, 0, 0]
+    assert oracle.walk_checksum(rp, col, [6, -1, 2], 1).tolist() == [0, 0, 7]
+    g = graphgen.config(1)
+    fr = np.arange(g.n, dtype=np.int32)
+    rp1 = g.row_ptr.astype(np.int64)
+    for P in (1, 2, 64, 256):
+        want = [(sum(P * (int(c) & ~(P - 1)) + P * (P - 1) // 2
+                     for c in g.col[rp1[u]:rp1[u + 1]])) % (1 << 32) for u in range(0, g.n, 7)]
+        assert oracle.walk_checksum(g.row_ptr, g.col, fr[::7], P).tolist() == want, P
+    for R in (3, 5, 37, 100):
+        want = [sum(_xor_sum_by_bits(int(c), R) for c in g.col[rp1[u]:rp1[u + 1]]) % (1 << 32)
+                for u in range(0, g.n, 11)]
+        assert oracle.walk_checksum(g.row_ptr, g.col, fr[::11], R).tolist() == want, R
+    # wrap-around: 40 entries of id 3 over 2^22 repeats sum to ~2^48
+    P = 1 << 22
+    rpw = np.array([0, 40, 40, 40, 40, 40], dtype=np.int64)
+    colw = np.full(40, 3, dtype=np.int32)
+    exact = 40 * (P * (3 & ~(P - 1)) + P * (P - 1) // 2)
+    assert exact >= 1 << 40
+    assert oracle.walk_checksum(rpw, colw, [0, 4], P).tolist() == [exact % (1 << 32), 0]
+
+
 def test_config1_eccentric_source_levels_equal_ecc_plus_one():
     g = graphgen.config(1)
     n = g.n
@@ -363,6 +412,8 @@ MUTANTS = [
      "edges += row_at(row_ptr, row_ptr_64, v + 1) + 0 *"),  # walked count without the row start
     ("row_at(row_ptr, row_ptr_64, v);\n        if (d > deepest)",
      "row_at(row_ptr, row_ptr_64, 0);\n        if (d > deepest)"),  # wrong row start
+    ("acc += (uint32_t)col[e] ^ (uint32_t)r;", "acc += (uint32_t)col[e] ^ (uint32_t)(r + 1);"),
+    ("acc += (uint32_t)col[e] ^ (uint32_t)r;", "acc += (uint32_t)col[e];"),  # XOR dropped
 ]
 
 
@@ -397,6 +448,8 @@ def test_pins_reject_oracle_mutants(old, new, golden, monkeypatch):
             "    ok = ok and oracle.level_sizes(np.array(g4['row_ptr']), d)[3] == 8\n"
             "d3, _, _ = oracle.bfs(rp, col, 3)\n"
             "ok = ok and oracle.level_sizes(rp, d3)[2:] == (3, 3)\n"
+            "ok = ok and oracle.walk_checksum(rp, col, [0, 3], 1).tolist() == [3, 9]\n"
+            "ok = ok and oracle.walk_checksum(rp, col, [0], 64).tolist() == [2 * 2016]\n"
             "print('PASS' if ok else 'FAIL')\n" % (tmp, gdir, gdir))
         out = subprocess.run(["python", "-c", code], capture_output=True, text=True,
                              timeout=120)
