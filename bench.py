@@ -643,26 +643,39 @@ def per_config(torch, fbc, graphgen, device, peak, rows_out, keep_rows=True):
     return out
 
 
+# name, options, (sources, timed repeats) when fewer than the default: the
+# thread-mapped padded advance walks a hub's whole row on one thread.
 ABLATION = [
-    ("auto_dir+auto_adv", dict()),
-    ("push_only+auto_adv", dict(direction=1)),
-    ("pull_only", dict(direction=2)),
-    ("push_only+binned", dict(direction=1, advance=1)),
-    ("push_only+merge_path", dict(direction=1, advance=2)),
-    ("auto_dir+binned", dict(advance=1)),
-    ("auto_dir+merge_path", dict(advance=2)),
+    ("auto_dir+merge_path(default)", dict(), None),
+    ("push_only+auto_adv", dict(direction=1), None),
+    ("pull_only", dict(direction=2), None),
+    ("push_only+binned", dict(direction=1, advance=1), None),
+    ("push_only+merge_path", dict(direction=1, advance=2), None),
+    ("auto_dir+binned", dict(advance=1), None),
+    ("auto_dir+hybrid_4096", dict(merge_path_min_frontier=4096), None),
+    ("discovery_cas", dict(discovery=1), None),
+    ("discovery_atomic_min", dict(discovery=2), None),
+    ("atomic_min+padded+filter", dict(discovery=2, frontier_output=1), None),
+    ("atomic_min+padded+filter+push_only", dict(discovery=2, frontier_output=1, direction=1), None),
+    ("atomic_min+padded_no_filter(thread_mapped,push_only)", dict(discovery=2, frontier_output=2),
+     (2, 1)),
+    ("parent_end_pass", dict(parent_pass=1), None),
+    ("parent_at_discovery", dict(parent_pass=2), None),
 ]
 
 
 def ablation(torch, fbc, graphgen, device, cases, nsrc=16, reps=3):
-    """Direction (push only, pull only, the automatic rule) and push advance
-    (degree-binned, merge path, the automatic hybrid that takes the merge path
-    from a 4,096-vertex frontier or an 8,192-degree hub) on the first 16
-    sources of each config: one search at a time (lanes = 1), GTEPS of a
+    """Direction (push only, pull only, the automatic rule), push advance
+    (degree-binned, merge path -- the default -- and the pages' static hybrid
+    that takes the merge path from a 4,096-vertex frontier or an 8,192-degree
+    hub), discovery (bitmap
+    atomicOr, atomicCAS, atomicMin on dist), the Gunrock-style padded frontier
+    with and without its filter, and where parents are written, on the first
+    16 sources of each config: one search at a time (lanes = 1), GTEPS of a
     bfs_csr_run_batch over the sources, median of `reps` timed batches after
     one warm-up. Each variant's distances are compared with the automatic
-    variant's (the option matrix of the tests checks every variant against
-    the oracle)."""
+    variant's rows (the option matrix of the tests checks every variant
+    against the oracle)."""
     out = {}
     stream = torch.cuda.current_stream(device)
     for cfg, g in cases:
@@ -673,19 +686,20 @@ def ablation(torch, fbc, graphgen, device, cases, nsrc=16, reps=3):
         k = len(srcs)
         dist = torch.empty((k, g.n), dtype=torch.int32, device=device)
         ref = None
-        edges = None
         res = {}
-        for name, over in ABLATION:
+        edge_rows = None
+        for name, over, limit in ABLATION:
+            kv, rv = (min(k, limit[0]), limit[1]) if limit else (k, reps)
             bfs = fbc.BfsCsr(row_ptr, col, symmetric=True, options=fbc.default_options(**over))
-            bfs.run_batch(srcs, dist, stream=stream)
-            if edges is None:
-                edges = sum(int(deg[dist[i] >= 0].sum().item()) for i in range(k))
+            bfs.run_batch(srcs[:kv], dist[:kv], stream=stream)
+            if edge_rows is None:
+                edge_rows = [int(deg[dist[i] >= 0].sum().item()) for i in range(k)]
             ts = []
-            for _ in range(reps):
+            for _ in range(rv):
                 e0 = torch.cuda.Event(enable_timing=True)
                 e1 = torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
-                bfs.run_batch(srcs, dist, stream=stream)
+                bfs.run_batch(srcs[:kv], dist[:kv], stream=stream)
                 e1.record(stream)
                 torch.cuda.synchronize(device)
                 ts.append(e0.elapsed_time(e1))
@@ -695,13 +709,15 @@ def ablation(torch, fbc, graphgen, device, cases, nsrc=16, reps=3):
                 ref = dist.clone()
                 same = True
             else:
-                same = bool(torch.equal(dist, ref))
-            res[name] = {"gteps": round(edges / (ms * 1e-3) / 1e9, 2),
-                         "ms_per_search": round(ms / k, 4), "same_dist_as_auto": same}
-        auto = res["auto_dir+auto_adv"]["gteps"]
+                same = bool(torch.equal(dist[:kv], ref[:kv]))
+            res[name] = {"gteps": round(sum(edge_rows[:kv]) / (ms * 1e-3) / 1e9, 2),
+                         "ms_per_search": round(ms / kv, 4), "sources": kv, "timed": rv,
+                         "same_dist_as_auto": same}
+        auto = res["auto_dir+merge_path(default)"]["gteps"]
         for name in res:
             res[name]["vs_auto"] = round(res[name]["gteps"] / auto, 3) if auto else None
         out[str(cfg)] = {"sources": k, "variants": res}
+        del edge_rows
         del dist, ref, row_ptr, col, row64, deg
         torch.cuda.empty_cache()
     return out
@@ -796,10 +812,12 @@ def walk_section(torch, fbc, graphgen, device, repeats=64, min_edges=1000):
 def per_level_overhead(torch, fbc, graphgen, device):
     """Per-level cost on graphs made of narrow levels: the 2048x2048 grid from
     its corner and a 10,000-vertex path (one vertex per level), in the
-    persistent loop and in the host loop (one launch + one device->host read
-    per level, the structure the Day 38 page measures). `*_us` is t_run per
-    level; `*_sync_us` is (t_run - sum of level busy times) / levels, busy =
-    last CTA's work end - level start from the level records."""
+    persistent loop, the CUDA-graph loop (one graph launch per search, a
+    device-driven while node launching one level per iteration) and the host
+    loop (one launch + one device->host read per level, the structure the
+    Day 38 page measures). The plain figure is t_run per level; `*_sync` is
+    (t_run - sum of level busy times) / levels, busy = last CTA's work end -
+    level start from the level records."""
     out = {}
     cases = [("grid_2048", graphgen.config(4)), ("path_10000", graphgen.path_graph(10000))]
     for name, g in cases:
@@ -809,11 +827,12 @@ def per_level_overhead(torch, fbc, graphgen, device):
         dist = torch.empty(g.n, dtype=torch.int32, device=device)
         row = {}
         for mode, loop in (("persistent", fbc.BFS_CSR_LOOP_PERSISTENT),
+                           ("graph_loop", fbc.BFS_CSR_LOOP_GRAPH),
                            ("host_loop", fbc.BFS_CSR_LOOP_HOST)):
             b = fbc.BfsCsr(rp, cl, True, fbc.default_options(loop_mode=loop))
             b.run(s, dist)
             levels = b.sync()
-            reps = 3 if loop == fbc.BFS_CSR_LOOP_PERSISTENT else 1
+            reps = 1 if loop == fbc.BFS_CSR_LOOP_HOST else 3
             best, best_busy = None, None
             for _ in range(reps):
                 torch.cuda.synchronize(device)
@@ -934,6 +953,66 @@ def cpu_leg(g, timed_rows, config_rows, graphgen, budget_s: float = 20.0):
     return base, cert
 
 
+# ------------------------------------------------------------------ profiler cases
+
+def run_profile_case(args):
+    """Small cases for a profiler (ncu), nothing timed or printed but a line
+    of what ran. 'levels': 3 warm-up searches, then --sources searches of
+    --config in the host loop mode, so that every level is its own
+    level_kernel launch. 'walk': the power-law graph's hub level (the level
+    whose frontier holds the largest degree, most eccentric source) walked
+    once by each mapping, 64 repeats."""
+    import torch
+
+    import frontier_bfs_csr_gb300 as fbc
+    import graphgen
+    device = torch.device("cuda", 0)
+    if args.profile == "levels":
+        g = graphgen.config(args.config)
+        row_ptr, col, _, _ = graph_tensors(torch, g, device)
+        bfs = fbc.BfsCsr(row_ptr, col, True, fbc.default_options(loop_mode=fbc.BFS_CSR_LOOP_HOST))
+        dist = torch.empty(g.n, dtype=torch.int32, device=device)
+        parent = torch.empty_like(dist)
+        s0 = int(g.sources[0])
+        for _ in range(3):
+            bfs.run(s0, dist, parent)
+            bfs.sync()
+        nsrc = args.sources if args.sources > 0 else 1
+        levels = []
+        for s in g.sources[:nsrc]:
+            bfs.run(int(s), dist, parent)
+            levels.append(bfs.sync())
+        bfs.close()
+        print(json.dumps({"profile": "levels", "config": args.config, "warmup_searches": 3,
+                          "levels_per_search": levels}))
+        return
+    g = graphgen.config(1)
+    row_ptr, col, _, deg = graph_tensors(torch, g, device)
+    bfs = fbc.BfsCsr(row_ptr, col, True)
+    dist = torch.empty(g.n, dtype=torch.int32, device=device)
+    lev = torch.empty(1, dtype=torch.int32, device=device)
+    best, best_levels = None, -1
+    for s in torch.nonzero(deg > 0).squeeze(1).tolist():
+        bfs.run(s, dist, None, lev)
+        L = int(lev.item())
+        if L > best_levels:
+            best, best_levels = s, L
+    bfs.run(best, dist)
+    bfs.sync()
+    d = dist.cpu().numpy()
+    dh = deg.cpu().numpy()
+    hub_level = max(range(best_levels), key=lambda k: int(dh[d == k].max()))
+    frontier = torch.from_numpy(np.nonzero(d == hub_level)[0].astype(np.int32)).to(device)
+    out = torch.empty(frontier.numel(), dtype=torch.int32, device=device)
+    for m in range(4):
+        bfs.walk(frontier, 64, m, out)
+    torch.cuda.synchronize(device)
+    bfs.close()
+    print(json.dumps({"profile": "walk", "source": best, "hub_level": hub_level,
+                      "frontier": int(frontier.numel()),
+                      "max_degree": int(dh[d == hub_level].max())}))
+
+
 # ------------------------------------------------------------------ reference arm
 
 def run_reference(args):
@@ -991,6 +1070,8 @@ def main():
                     help="skip the direction / advance ablation")
     ap.add_argument("--no-walk", action="store_true",
                     help="skip the isolated-level walk of the power-law graph")
+    ap.add_argument("--profile", choices=["levels", "walk"], default=None,
+                    help="run a small case for a profiler and exit (see run_profile_case)")
     ap.add_argument("--lanes", type=int, default=2,
                     help="searches bfs_csr_run_batch keeps in flight (1..8)")
     ap.add_argument("--sources", type=int, default=0,
@@ -998,7 +1079,9 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
-    if args.impl == "reference":
+    if args.profile is not None:
+        run_profile_case(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -36,8 +36,11 @@ BFS_CSR_EDEVICE = 6
 
 BFS_CSR_DIR_AUTO, BFS_CSR_DIR_PUSH, BFS_CSR_DIR_PULL = 0, 1, 2
 BFS_CSR_ADV_AUTO, BFS_CSR_ADV_BINNED, BFS_CSR_ADV_MERGE_PATH, BFS_CSR_ADV_SINGLE_CTA = 0, 1, 2, 3
-BFS_CSR_DISC_BITMAP, BFS_CSR_DISC_CAS = 0, 1
-BFS_CSR_LOOP_PERSISTENT, BFS_CSR_LOOP_HOST = 0, 1
+BFS_CSR_ADV_PADDED = 4
+BFS_CSR_DISC_BITMAP, BFS_CSR_DISC_CAS, BFS_CSR_DISC_MIN = 0, 1, 2
+BFS_CSR_FRONTIER_COMPACT, BFS_CSR_FRONTIER_PADDED_FILTER, BFS_CSR_FRONTIER_PADDED = 0, 1, 2
+BFS_CSR_LOOP_PERSISTENT, BFS_CSR_LOOP_HOST, BFS_CSR_LOOP_GRAPH = 0, 1, 2
+BFS_CSR_PARENT_AUTO, BFS_CSR_PARENT_END_PASS, BFS_CSR_PARENT_AT_DISCOVERY = 0, 1, 2
 BFS_CSR_WALK_THREAD, BFS_CSR_WALK_WARP, BFS_CSR_WALK_BINNED, BFS_CSR_WALK_EDGE = 0, 1, 2, 3
 
 EXPORTED = [
@@ -70,7 +73,9 @@ class bfs_csr_options(ctypes.Structure):
         ("push_beta", ctypes.c_int32),
         ("narrow_max_edges", ctypes.c_int32),
         ("lanes", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 4),
+        ("parent_pass", ctypes.c_int32),
+        ("frontier_output", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 2),
     ]
 
 

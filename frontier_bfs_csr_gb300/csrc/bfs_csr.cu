@@ -29,18 +29,21 @@ constexpr int kDefaultBlock = 512;
 
 constexpr int kMaxLanes = 8;
 
-// Workspace: the graph part (dead bitmap, head array), derived once per CSR,
+// Workspace: the graph part (dead bitmap, probe array), derived once per CSR,
 // then one search part per lane; the offsets below are lane 0's, lane j's
 // are `search` bytes further on.
 struct Layout {
-    size_t dead, head;
-    size_t ctl, visited, hop, fb0, fb1, qv0, qv1, qbeg0, qbeg1, qoff0, qoff1, stats;
+    size_t dead, probe;
+    size_t ctl, visited, hop, fb0, fb1, qv0, qv1, qbeg0, qbeg1, qoff0, qoff1, stats, pad0, pad1;
+    size_t pad_entries;
     size_t search, total;
 };
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-Layout make_layout(int64_t n, int row_ptr_64, int lanes = 1)
+// pad_entries: length of each padded-frontier array (0 without the padded
+// frontier modes).
+Layout make_layout(int64_t n, int row_ptr_64, int lanes = 1, size_t pad_entries = 0)
 {
     Layout L;
     const size_t words = (size_t)((n + 31) / 32);
@@ -52,7 +55,7 @@ Layout make_layout(int64_t n, int row_ptr_64, int lanes = 1)
         return at;
     };
     L.dead = take(words * 4);
-    L.head = take((size_t)n * 8);
+    L.probe = take((size_t)n * 4);
     const size_t search0 = off;
     L.ctl = take(sizeof(Ctl));
     L.visited = take(words * 4);
@@ -66,9 +69,19 @@ Layout make_layout(int64_t n, int row_ptr_64, int lanes = 1)
     L.qoff0 = take((size_t)n * R);
     L.qoff1 = take((size_t)n * R);
     L.stats = take((size_t)kStatsCap * sizeof(bfs_csr_level_stat));
+    L.pad_entries = pad_entries;
+    L.pad0 = pad_entries ? take(pad_entries * 4) : 0;
+    L.pad1 = pad_entries ? take(pad_entries * 4) : 0;
     L.search = off - search0;
     L.total = off + (size_t)(lanes - 1) * L.search;
     return L;
+}
+
+size_t pad_entries_for(const bfs_csr_options& o, int64_t nnz)
+{
+    if (o.frontier_output == BFS_CSR_FRONTIER_COMPACT)
+        return 0;
+    return (size_t)(nnz > 0 ? nnz : 1);
 }
 
 }  // namespace
@@ -88,6 +101,7 @@ struct bfs_csr_t {
     int eb = 0;
     int device = 0;
     int sm_count = 0;
+    int l2_bytes = 0;
     int block = kDefaultBlock;
     int grid = 0;
     size_t smem = 0;
@@ -114,6 +128,15 @@ struct bfs_csr_t {
     cudaStream_t copy_stream = nullptr;
     cudaEvent_t ev_search[2] = {nullptr, nullptr};
     cudaEvent_t ev_copy[2] = {nullptr, nullptr};
+    // graph loop mode: one instantiated graph per (lane, outputs, stamps),
+    // made on first use and kept until destroy
+    struct LoopGraph {
+        int lane = 0, grid = 0;
+        const void *dist = nullptr, *parent = nullptr, *levels = nullptr, *stamps = nullptr;
+        cudaGraph_t graph = nullptr;
+        cudaGraphExec_t exec = nullptr;
+    };
+    std::vector<LoopGraph> graphs;
     // device batches: one stream per lane and the fork/join events (made on
     // first use)
     int lanes = 1;
@@ -144,8 +167,10 @@ int check_options(const bfs_csr_options& o)
 {
     if (o.direction < BFS_CSR_DIR_AUTO || o.direction > BFS_CSR_DIR_PULL) return BFS_CSR_EINVAL;
     if (o.advance < BFS_CSR_ADV_AUTO || o.advance > BFS_CSR_ADV_MERGE_PATH) return BFS_CSR_EINVAL;
-    if (o.discovery < BFS_CSR_DISC_BITMAP || o.discovery > BFS_CSR_DISC_CAS) return BFS_CSR_EINVAL;
-    if (o.loop_mode < BFS_CSR_LOOP_PERSISTENT || o.loop_mode > BFS_CSR_LOOP_HOST) return BFS_CSR_EINVAL;
+    if (o.discovery < BFS_CSR_DISC_BITMAP || o.discovery > BFS_CSR_DISC_MIN) return BFS_CSR_EINVAL;
+    if (o.frontier_output < BFS_CSR_FRONTIER_COMPACT || o.frontier_output > BFS_CSR_FRONTIER_PADDED)
+        return BFS_CSR_EINVAL;
+    if (o.loop_mode < BFS_CSR_LOOP_PERSISTENT || o.loop_mode > BFS_CSR_LOOP_GRAPH) return BFS_CSR_EINVAL;
     if (o.small_max_degree < 1 || o.cta_min_degree < o.small_max_degree) return BFS_CSR_EINVAL;
     if (o.merge_path_min_frontier < 0 || o.binned_max_degree < 1) return BFS_CSR_EINVAL;
     if (!(o.pull_alpha >= 0.0) || o.push_beta < 0) return BFS_CSR_EINVAL;
@@ -154,6 +179,8 @@ int check_options(const bfs_csr_options& o)
     if (o.grid_blocks < 0 || o.barrier_timeout_ns <= 0 || o.narrow_max_edges < 0)
         return BFS_CSR_EINVAL;
     if (o.lanes < 0 || o.lanes > kMaxLanes)
+        return BFS_CSR_EINVAL;
+    if (o.parent_pass < BFS_CSR_PARENT_AUTO || o.parent_pass > BFS_CSR_PARENT_AT_DISCOVERY)
         return BFS_CSR_EINVAL;
     return BFS_CSR_OK;
 }
@@ -208,9 +235,15 @@ Params<RowT> make_params(bfs_csr_t* h, int32_t* d_dist, int32_t* d_parent, int32
     p.parent = d_parent;
     p.visited = reinterpret_cast<uint32_t*>(w + h->L.visited);
     p.dead = reinterpret_cast<const uint32_t*>(g + h->L.dead);
-    p.head = reinterpret_cast<const int2*>(g + h->L.head);
+    p.probe = reinterpret_cast<const uint32_t*>(g + h->L.probe);
     p.hop = reinterpret_cast<uint8_t*>(w + h->L.hop);
     p.defer_dist = h->opt.discovery == BFS_CSR_DISC_BITMAP ? 1 : 0;
+    // A parent array within half of the L2 takes scattered stores without
+    // DRAM read-modify-writes; a larger one is written once, whole, by the
+    // end-of-search pass (R-MAT scale 25: 134 MB against a 129 MB L2).
+    const bool big = (size_t)h->n * 4 > (size_t)h->l2_bytes / 2;
+    p.defer_parent = p.defer_dist && (h->opt.parent_pass == BFS_CSR_PARENT_END_PASS ||
+                                      (h->opt.parent_pass == BFS_CSR_PARENT_AUTO && big)) ? 1 : 0;
     p.vec_out = ((reinterpret_cast<uintptr_t>(d_dist) & 15u) == 0 &&
                  (reinterpret_cast<uintptr_t>(d_parent) & 15u) == 0) ? 1 : 0;
     p.fb[0] = reinterpret_cast<uint32_t*>(w + h->L.fb0);
@@ -222,6 +255,10 @@ Params<RowT> make_params(bfs_csr_t* h, int32_t* d_dist, int32_t* d_parent, int32
     p.qoff[0] = reinterpret_cast<RowT*>(w + h->L.qoff0);
     p.qoff[1] = reinterpret_cast<RowT*>(w + h->L.qoff1);
     p.ctl = reinterpret_cast<Ctl*>(w + h->L.ctl);
+    p.frontier_output = h->opt.frontier_output;
+    p.emit_max = 65536;
+    p.pad[0] = h->L.pad_entries ? reinterpret_cast<int32_t*>(w + h->L.pad0) : nullptr;
+    p.pad[1] = h->L.pad_entries ? reinterpret_cast<int32_t*>(w + h->L.pad1) : nullptr;
     p.stats = reinterpret_cast<bfs_csr_level_stat*>(w + h->L.stats);
     p.stats_cap = kStatsCap;
     p.num_levels_out = d_levels;
@@ -242,7 +279,7 @@ Params<RowT> make_params(bfs_csr_t* h, int32_t* d_dist, int32_t* d_parent, int32
     p.timeout_ns = h->opt.barrier_timeout_ns;
     p.unreachable_barrier = h->opt.test_unreachable_barrier ? 1 : 0;
     {
-        const int cap = h->block * fbc::kItems;
+        const int cap = fbc::stage_cap<RowT>(h->block);
         p.narrow_max = h->opt.narrow_max_edges < cap ? h->opt.narrow_max_edges : cap;
     }
     return p;
@@ -278,8 +315,8 @@ int prepare(bfs_csr_t* h, cudaStream_t s)
         FBC_CUDA(h, cudaMemcpyAsync(&cj->nonisolated, &ctl->nonisolated, sizeof(long long),
                                     cudaMemcpyDeviceToDevice, s));
     }
-    fbc::head_kernel<RowT><<<init_grid(h), 256, 0, s>>>(rp, h->col, (int32_t)h->n,
-                                                         reinterpret_cast<int2*>(w + h->L.head));
+    fbc::probe_kernel<RowT><<<init_grid(h), 256, 0, s>>>(rp, h->col, (int32_t)h->n,
+                                                          reinterpret_cast<uint32_t*>(w + h->L.probe));
     FBC_CUDA(h, cudaGetLastError());
     FBC_CUDA(h, cudaStreamSynchronize(s));
     return configure_grid<RowT>(h);
@@ -297,6 +334,91 @@ int launch_init(bfs_csr_t* h, int32_t source, int32_t* d_dist, int32_t* d_parent
     return BFS_CSR_OK;
 }
 
+constexpr size_t kMaxLoopGraphs = 64;
+
+// Graph loop mode: a CUDA graph whose one node is a while loop; its body is
+// one cooperative launch of the level kernel with a budget of one level.
+// The kernel's last CTA sets the loop's condition to 0 once the search has
+// ended (or failed), so one graph launch runs the whole level loop with no
+// host round trip. The graph holds the kernel's parameters (outputs and
+// stamps included), so it is made once per set of them and kept.
+template <typename RowT>
+int loop_graph(bfs_csr_t* h, int32_t* d_dist, int32_t* d_parent, int32_t* d_levels, int lane,
+               int grid, long long* stamps, cudaGraphExec_t* out)
+{
+    for (const auto& g : h->graphs) {
+        if (g.lane == lane && g.grid == grid && g.dist == d_dist && g.parent == d_parent &&
+            g.levels == d_levels && g.stamps == stamps) {
+            *out = g.exec;
+            return BFS_CSR_OK;
+        }
+    }
+    if (h->graphs.size() >= kMaxLoopGraphs) {
+        auto& old = h->graphs.front();
+        cudaGraphExecDestroy(old.exec);
+        cudaGraphDestroy(old.graph);
+        h->graphs.erase(h->graphs.begin());
+    }
+    bfs_csr_t::LoopGraph lg;
+    lg.lane = lane;
+    lg.grid = grid;
+    lg.dist = d_dist;
+    lg.parent = d_parent;
+    lg.levels = d_levels;
+    lg.stamps = stamps;
+    FBC_CUDA(h, cudaGraphCreate(&lg.graph, 0));
+    auto fail = [&](cudaError_t e) {
+        cudaGraphDestroy(lg.graph);
+        return cuda_fail(h, e);
+    };
+    cudaGraphConditionalHandle cond = 0;
+    cudaError_t e = cudaGraphConditionalHandleCreate(&cond, lg.graph, 1u, cudaGraphCondAssignDefault);
+    if (e != cudaSuccess)
+        return fail(e);
+    // cudaGraphNodeParams has no default constructor (its union holds dim3s):
+    // build it in zeroed storage, as its reserved fields require.
+    alignas(cudaGraphNodeParams) unsigned char cbuf[sizeof(cudaGraphNodeParams)] = {};
+    cudaGraphNodeParams& cp = *reinterpret_cast<cudaGraphNodeParams*>(cbuf);
+    cp.type = cudaGraphNodeTypeConditional;
+    cp.conditional.handle = cond;
+    cp.conditional.type = cudaGraphCondTypeWhile;
+    cp.conditional.size = 1;
+    cudaGraphNode_t cnode = nullptr;
+    e = cudaGraphAddNode(&cnode, lg.graph, nullptr, nullptr, 0, &cp);
+    if (e != cudaSuccess)
+        return fail(e);
+    cudaGraph_t body = cp.conditional.phGraph_out[0];
+    Params<RowT> p = make_params<RowT>(h, d_dist, d_parent, d_levels, lane);
+    p.stamps = stamps;
+    p.level_budget = 1;
+    p.graph_cond = cond;
+    void* args[] = {&p};
+    alignas(cudaGraphNodeParams) unsigned char kbuf[sizeof(cudaGraphNodeParams)] = {};
+    cudaGraphNodeParams& kp = *reinterpret_cast<cudaGraphNodeParams*>(kbuf);
+    kp.type = cudaGraphNodeTypeKernel;
+    kp.kernel.func = level_kernel_ptr<RowT>();
+    kp.kernel.gridDim = dim3(grid);
+    kp.kernel.blockDim = dim3(h->block);
+    kp.kernel.sharedMemBytes = (unsigned)h->smem;
+    kp.kernel.kernelParams = args;
+    cudaGraphNode_t knode = nullptr;
+    e = cudaGraphAddNode(&knode, body, nullptr, nullptr, 0, &kp);
+    if (e != cudaSuccess)
+        return fail(e);
+    cudaLaunchAttributeValue coop;
+    std::memset(&coop, 0, sizeof(coop));
+    coop.cooperative = 1;
+    e = cudaGraphKernelNodeSetAttribute(knode, cudaLaunchAttributeCooperative, &coop);
+    if (e != cudaSuccess)
+        return fail(e);
+    e = cudaGraphInstantiate(&lg.exec, lg.graph, 0);
+    if (e != cudaSuccess)
+        return fail(e);
+    h->graphs.push_back(lg);
+    *out = lg.exec;
+    return BFS_CSR_OK;
+}
+
 template <typename RowT>
 int launch_levels(bfs_csr_t* h, int32_t* d_dist, int32_t* d_parent, int32_t* d_levels,
                   cudaStream_t s, int lane = 0, int grid = 0, long long* stamps = nullptr)
@@ -309,6 +431,14 @@ int launch_levels(bfs_csr_t* h, int32_t* d_dist, int32_t* d_parent, int32_t* d_l
     if (h->opt.loop_mode == BFS_CSR_LOOP_PERSISTENT) {
         FBC_CUDA(h, cudaLaunchCooperativeKernel(level_kernel_ptr<RowT>(), dim3(grid),
                                                 dim3(h->block), args, h->smem, s));
+        return BFS_CSR_OK;
+    }
+    if (h->opt.loop_mode == BFS_CSR_LOOP_GRAPH) {
+        cudaGraphExec_t exec = nullptr;
+        const int rc = loop_graph<RowT>(h, d_dist, d_parent, d_levels, lane, grid, stamps, &exec);
+        if (rc != BFS_CSR_OK)
+            return rc;
+        FBC_CUDA(h, cudaGraphLaunch(exec, s));
         return BFS_CSR_OK;
     }
     // Host loop: one launch per level and a device->host read of the state.
@@ -329,7 +459,7 @@ int launch_levels(bfs_csr_t* h, int32_t* d_dist, int32_t* d_parent, int32_t* d_l
 int create_common(bfs_csr_t* h, void* d_workspace, size_t workspace_bytes, cudaStream_t s)
 {
     h->lanes = h->opt.lanes > 1 ? h->opt.lanes : 1;
-    h->L = make_layout(h->n, h->row_ptr_64, h->lanes);
+    h->L = make_layout(h->n, h->row_ptr_64, h->lanes, pad_entries_for(h->opt, h->nnz));
     h->words = (int)((h->n + 31) / 32);
     if (d_workspace != nullptr) {
         if (workspace_bytes < h->L.total || (reinterpret_cast<uintptr_t>(d_workspace) & 255u))
@@ -384,6 +514,10 @@ void release(bfs_csr_t* h)
         if (h->ev_join[j]) cudaEventDestroy(h->ev_join[j]);
     }
     if (h->ev_fork) cudaEventDestroy(h->ev_fork);
+    for (auto& g : h->graphs) {
+        if (g.exec) cudaGraphExecDestroy(g.exec);
+        if (g.graph) cudaGraphDestroy(g.graph);
+    }
     delete h;
 }
 
@@ -401,6 +535,7 @@ int init_handle(bfs_csr_t* h, int64_t n, int64_t nnz, int row_ptr_64, int symmet
     h->eb = edge_bits(n, nnz, h->row_ptr_64);
     FBC_CUDA(h, cudaGetDevice(&h->device));
     FBC_CUDA(h, cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, h->device));
+    FBC_CUDA(h, cudaDeviceGetAttribute(&h->l2_bytes, cudaDevAttrL2CacheSize, h->device));
     int coop = 0;
     FBC_CUDA(h, cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, h->device));
     if (!coop)
@@ -418,7 +553,7 @@ int upload_host_csr(bfs_csr_t* h, const void* h_row_ptr, const int32_t* h_col, c
         FBC_CUDA(h, cudaMemcpyAsync(h->d_col_own, h_col, (size_t)h->nnz * 4,
                                     cudaMemcpyHostToDevice, s));
     // A new CSR: validate it and re-derive the dead bitmap, the non-isolated
-    // count and the head array, as create does.
+    // count and the probe array, as create does.
     return h->row_ptr_64 ? prepare<int64_t>(h, s) : prepare<int32_t>(h, s);
 }
 
@@ -437,7 +572,7 @@ int bfs_csr_default_options(bfs_csr_options* o)
     o->loop_mode = BFS_CSR_LOOP_PERSISTENT;
     o->small_max_degree = 32;
     o->cta_min_degree = 256;
-    o->merge_path_min_frontier = 4096;
+    o->merge_path_min_frontier = 0;
     o->binned_max_degree = 8192;
     o->pull_alpha = 14.0;
     o->push_beta = 24;
@@ -461,7 +596,9 @@ int bfs_csr_workspace_bytes(int64_t n, int64_t nnz, int row_ptr_64, const bfs_cs
     if (rc != BFS_CSR_OK)
         return rc;
     const int lanes = opt != nullptr && opt->lanes > 1 ? opt->lanes : 1;
-    *bytes = make_layout(n, row_ptr_64, lanes).total;
+    bfs_csr_options d;
+    bfs_csr_default_options(&d);
+    *bytes = make_layout(n, row_ptr_64, lanes, pad_entries_for(opt != nullptr ? *opt : d, nnz)).total;
     return BFS_CSR_OK;
 }
 
@@ -943,7 +1080,7 @@ constexpr int64_t kNoAllocMaxN = BFS_CSR_NOALLOC_MAX_VERTICES;
 // to 256 bytes.
 constexpr size_t kNoAllocBytes =
     (sizeof(Ctl) + 256) + 4 * ((size_t)kNoAllocMaxN / 8 + 256) +
-    ((size_t)kNoAllocMaxN * 8 + 256) + ((size_t)kNoAllocMaxN + 256) +
+    ((size_t)kNoAllocMaxN * 4 + 256) + ((size_t)kNoAllocMaxN + 256) +
     2 * ((size_t)kNoAllocMaxN * 4 + 256) + 4 * ((size_t)kNoAllocMaxN * 4 + 256) +
     ((size_t)kStatsCap * sizeof(bfs_csr_level_stat) + 256);
 
@@ -992,6 +1129,10 @@ extern "C" int bfs_csr_run_noalloc(int64_t n, int64_t nnz, const int32_t* d_row_
         return BFS_CSR_EUNSUPPORTED;
     if (h.opt.lanes > 1)
         return BFS_CSR_EUNSUPPORTED;  // the scratch array holds one search's state
+    if (h.opt.loop_mode == BFS_CSR_LOOP_GRAPH)
+        return BFS_CSR_EUNSUPPORTED;  // a graph is a resource this entry point cannot keep
+    if (h.opt.frontier_output != BFS_CSR_FRONTIER_COMPACT)
+        return BFS_CSR_EUNSUPPORTED;  // the padded arrays (nnz entries each) do not fit the scratch
     void* scratch = nullptr;
     rc = noalloc_scratch(h.device, &scratch);
     if (rc != BFS_CSR_OK)

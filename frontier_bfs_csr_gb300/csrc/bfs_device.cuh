@@ -47,6 +47,24 @@
 namespace fbc {
 
 constexpr int kItems = 4;        // edges per thread per single-CTA level round
+
+// Single-CTA level capacities, in entries. The stage holds the next frontier
+// (and is the CTA stage of the grid-wide compaction); a single-CTA level's
+// edges are bounded by it, so its winners always fit. The window holds the
+// current frontier. Both are one round of kItems edges per thread: a wider
+// stage (7,168 entries with 4-byte row offsets, several rounds per level)
+// made the lattice's levels slower on one CTA than on the whole grid, and
+// its shared memory took L1 capacity from the other configurations.
+template <typename RowT>
+__host__ __device__ constexpr int stage_cap(int bd)
+{
+    return kItems * bd;
+}
+
+__host__ __device__ constexpr int window_cap(int bd)
+{
+    return kItems * bd;
+}
 constexpr int kSlots = 4;        // rotating per-level counter slots
 constexpr int kMaxBlock = 1024;
 constexpr unsigned kFull = 0xffffffffu;
@@ -93,15 +111,25 @@ struct Params {
     int32_t words;              // ceil(n / 32)
     int32_t* dist;
     int32_t* parent;            // may be null
-    // Hop code per vertex while a search runs (bitmap discovery only): 0
-    // unreached, d + 1 for a distance d < kHopDirect, kHopFar when the
-    // distance itself went straight to dist. dist is written from it once,
-    // coalesced, when the search ends.
+    // Hop code per vertex while a search runs (bitmap discovery only): the
+    // low 7 bits are 0 unreached, d + 1 for a distance d < kHopDirect,
+    // kHopFar when the distance itself went straight to dist; the top bit
+    // says the parent is the vertex's probe neighbour (probe[]) and was not
+    // stored. dist and parent are written from the codes once, coalesced,
+    // when the search ends.
     uint8_t* hop;
-    int defer_dist;             // 1: discoveries write hop, not dist
+    int defer_dist;             // 1: discoveries write hop codes (bitmap discovery)
+    // 1 (only with defer_dist): a pull level's probe hits store no parent;
+    // the end-of-search pass writes every parent from the hop-code flags. Set
+    // when the parent array is too large for the L2 to absorb scattered
+    // stores into it.
+    int defer_parent;
     uint32_t* visited;
     const uint32_t* dead;       // degree-0 vertices and padding bits (symmetric CSR)
-    const int2* head;           // per vertex: (first neighbour or -1, degree)
+    // Per vertex: its probe neighbour (the highest-degree one among the row's
+    // first entries) in bits 0-30, kProbeNone for a row without entries,
+    // and bit 31 set when that neighbour is the row's only entry.
+    const uint32_t* probe;
     int vec_out;                // dist and parent are 16-byte aligned
     uint32_t* fb[2];            // frontier bitmaps, F_k in fb[k & 1]
     int32_t* qv[2];             // frontier queues, F_k in qv[k & 1]
@@ -124,6 +152,17 @@ struct Params {
     int unreachable_barrier;
     int narrow_max;             // single-CTA levels: frontier edges (and vertices) <= this
     long long* stamps;          // may be null: global timer at init, level-loop start and end
+    // BFS_CSR_FRONTIER_*: how a push level hands its winners to the next
+    // level; the padded modes use pad[] (max(nnz, 1) entries each).
+    int frontier_output;
+    int32_t* pad[2];
+    // A pull level that starts with at most this many unvisited vertices also
+    // appends what it finds to the next queue, so that a push level after it
+    // needs no bitmap-to-queue pass.
+    long long emit_max;
+    // Graph loop mode: the conditional handle of the CUDA graph's while node
+    // whose body launches this kernel once per level (0 otherwise).
+    unsigned long long graph_cond;
 };
 
 // ------------------------------------------------------------ primitives
@@ -283,6 +322,8 @@ struct __align__(16) SmemScalars {
 };
 
 // Per-thread tallies of the vertices this thread discovered in a level.
+// Push levels count the found vertices' out-degrees in `edges`; pull levels
+// count there the out-degrees of the unvisited vertices they did not find.
 struct Tally {
     unsigned long long found;
     unsigned long long edges;
@@ -379,9 +420,13 @@ __device__ void stage_flush(const Params<RowT>& p, const Smem<RowT>& sm, SmemSca
     __syncthreads();
 }
 
-// End of a level: one atomic per CTA for each frontier statistic.
+// End of a level: one atomic per CTA for each frontier statistic. After a
+// pull level (`pulled`) fedges accumulates minus the edges of the vertices
+// left unvisited, so that the next level reads m_F = m_U - that sum: the
+// unvisited vertices at the level's start are exactly the ones it found plus
+// the ones it did not.
 template <typename RowT>
-__device__ void publish_tally(const Tally& t, LevelSlot* nxt, SmemScalars& ss)
+__device__ void publish_tally(const Tally& t, LevelSlot* nxt, SmemScalars& ss, bool pulled)
 {
     long long tot_found, tot_edges;
     block_exclusive_scan((long long)t.found, &tot_found, ss.tmp_ll);
@@ -396,8 +441,12 @@ __device__ void publish_tally(const Tally& t, LevelSlot* nxt, SmemScalars& ss)
         unsigned long long mm = 0;
         for (int w = 0; w < (int)((blockDim.x + 31) >> 5); ++w)
             mm = s_max[w] > mm ? s_max[w] : mm;
-        if (tot_found > 0) {
+        if (tot_found > 0)
             atomicAdd(&nxt->found, (unsigned long long)tot_found);
+        if (pulled) {
+            if (tot_edges != 0)
+                atomicAdd(&nxt->fedges, (unsigned long long)(-tot_edges));
+        } else if (tot_found > 0) {
             atomicAdd(&nxt->fedges, (unsigned long long)tot_edges);
             atomicMax(&nxt->maxdeg, mm);
         }
@@ -411,18 +460,26 @@ __device__ void publish_tally(const Tally& t, LevelSlot* nxt, SmemScalars& ss)
 // search: a discovery then touches one byte of an array an eighth the size
 // of dist (it mostly stays in L2) instead of a 4-byte slot of a 32-byte DRAM
 // sector that must be read, merged and written back. Larger distances (long
-// paths, lattices) go to dist directly and are marked kHopFar.
-constexpr int kHopDirect = 254;
-constexpr uint8_t kHopFar = 255;
+// paths, lattices) go to dist directly and are marked kHopFar. The top bit,
+// kHopProbe, marks a vertex whose parent is its probe neighbour: almost
+// every vertex a pull level finds (the probe is the one neighbour it tests
+// first), so its parent costs no scattered store either and is written by
+// the end-of-search pass from probe[], sequentially.
+constexpr int kHopDirect = 126;
+constexpr uint8_t kHopFar = 127;
+constexpr uint8_t kHopProbe = 0x80;
+constexpr uint32_t kProbeNone = 0x7fffffffu;
 
 template <typename RowT>
-__device__ __forceinline__ void record_dist(const Params<RowT>& p, int32_t v, int d)
+__device__ __forceinline__ void record_dist(const Params<RowT>& p, int32_t v, int d,
+                                            bool probe_parent = false)
 {
     if (p.defer_dist) {
+        const uint8_t flag = probe_parent ? kHopProbe : (uint8_t)0;
         if (d < kHopDirect) {
-            p.hop[v] = (uint8_t)(d + 1);
+            p.hop[v] = (uint8_t)(d + 1) | flag;
         } else {
-            p.hop[v] = kHopFar;
+            p.hop[v] = kHopFar | flag;
             p.dist[v] = d;
         }
     } else {
@@ -431,7 +488,17 @@ __device__ __forceinline__ void record_dist(const Params<RowT>& p, int32_t v, in
 }
 
 // The claim of vertex v by frontier vertex u at level k. Exactly one caller
-// per v gets true; the winner writes dist[v] and parent[v].
+// per v gets true; the winner writes dist[v] and parent[v]. With
+// BFS_CSR_DISC_MIN the claim is an atomic minimum of dist[v], read as an
+// unsigned word so that the unvisited -1 is the largest value: the first
+// caller sees the old -1 and wins, any later one sees level + 1 and loses
+// (the Gunrock page, step 2); min is idempotent, so every interleaving
+// leaves the same dist.
+__device__ __forceinline__ unsigned int* as_unsigned(int32_t* x)
+{
+    return reinterpret_cast<unsigned int*>(x);
+}
+
 template <typename RowT>
 __device__ __forceinline__ bool claim(const Params<RowT>& p, int k, int32_t v, int32_t u,
                                       bool precheck)
@@ -440,6 +507,13 @@ __device__ __forceinline__ bool claim(const Params<RowT>& p, int k, int32_t v, i
         if (precheck && ldcg(&p.dist[v]) != -1)
             return false;
         if (atomicCAS(&p.dist[v], -1, k + 1) != -1)
+            return false;
+        atomicOr(&p.visited[v >> 5], 1u << (v & 31));  // keeps pull levels exact
+    } else if (p.discovery == BFS_CSR_DISC_MIN) {
+        const unsigned int d = (unsigned int)(k + 1);
+        if (precheck && (unsigned int)ldcg(&p.dist[v]) <= d)
+            return false;
+        if (!(d < atomicMin(as_unsigned(p.dist + v), d)))
             return false;
         atomicOr(&p.visited[v >> 5], 1u << (v & 31));  // keeps pull levels exact
     } else {
@@ -475,6 +549,21 @@ __device__ __forceinline__ void claim_batch(const Params<RowT>& p, int k, const 
         for (int i = 0; i < N; ++i)
             if (won[i])
                 atomicOr(&p.visited[v[i] >> 5], 1u << (v[i] & 31));
+    } else if (p.discovery == BFS_CSR_DISC_MIN) {
+        const unsigned int d = (unsigned int)(k + 1);
+        unsigned int seen[N], old[N];
+#pragma unroll
+        for (int i = 0; i < N; ++i)
+            seen[i] = (v[i] >= 0 && precheck) ? (unsigned int)ldcg(&p.dist[v[i]]) : 0xffffffffu;
+#pragma unroll
+        for (int i = 0; i < N; ++i)
+            old[i] = (v[i] >= 0 && seen[i] > d) ? atomicMin(as_unsigned(p.dist + v[i]), d) : 0u;
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            won[i] = v[i] >= 0 && d < old[i];
+            if (won[i])
+                atomicOr(&p.visited[v[i] >> 5], 1u << (v[i] & 31));
+        }
     } else {
         uint32_t seen[N];
 #pragma unroll
@@ -812,6 +901,19 @@ __device__ void push_warp_mp(const Params<RowT>& p, int k, int qn, RowT qm, unsi
         }
         bool won[kWItems];
         claim_batch(p, k, vv, uu, pre, won);
+        if (p.frontier_output == BFS_CSR_FRONTIER_PADDED_FILTER) {
+            // Every edge of the level writes its slot of the padded output:
+            // the neighbour it claimed, or the sentinel -1 (the filter pass
+            // compacts them).
+#pragma unroll
+            for (int j = 0; j < kWItems; ++j) {
+                const long long ej = e + 32 * j + lane;
+                if (j < n && ej < e_hi)
+                    p.pad[0][ej] = won[j] ? vv[j] : -1;
+            }
+            e += 32 * n;
+            continue;
+        }
         RowT wb[kWItems], we[kWItems];
 #pragma unroll
         for (int j = 0; j < kWItems; ++j) {
@@ -846,9 +948,86 @@ __device__ void push_warp_mp(const Params<RowT>& p, int k, int qn, RowT qm, unsi
         warp_flush(p, ws, cnt, nxt, ns);
 }
 
+// ------------------------------------------------------------ padded frontiers
+
+// The filter of the Gunrock page, step 2: the padded output pad[0][0, L) of
+// a push level (one slot per frontier edge: a claimed neighbour or -1) is
+// compacted into the next queue through the CTA stage, and the new
+// frontier's statistics are counted. Every thread of the grid calls it.
+template <typename RowT>
+__device__ void filter_padded(const Params<RowT>& p, unsigned long long L, const Smem<RowT>& sm,
+                              SmemScalars& ss, LevelSlot* nxt, int qsel, Tally& t)
+{
+    const int32_t* in = p.pad[0];
+    const unsigned long long bd = blockDim.x;
+    const unsigned long long stride = (unsigned long long)gridDim.x * bd;
+    for (unsigned long long base = blockIdx.x * bd; base < L; base += stride) {
+        const unsigned long long i = base + threadIdx.x;
+        const int32_t v = i < L ? ldcg(in + i) : -1;
+        RowT b = 0, deg = 0;
+        if (v >= 0) {
+            b = p.row_ptr[v];
+            deg = p.row_ptr[v + 1] - b;
+            t.found += 1;
+            t.edges += (unsigned long long)deg;
+            t.maxdeg = (unsigned long long)deg > t.maxdeg ? (unsigned long long)deg : t.maxdeg;
+        }
+        stage_push(p, sm, ss, nxt, qsel, v, b, deg, v >= 0 && deg > 0);
+        if (__syncthreads_or(ss.stage_n > sm.cap / 2))
+            stage_flush(p, sm, ss, nxt, qsel);
+    }
+    stage_flush(p, sm, ss, nxt, qsel);
+}
+
+// A push level without the filter: the frontier is the padded array
+// pad[k & 1][0, L) of the previous level, sentinels included, and each
+// thread takes one slot and walks its vertex's whole row (the thread-mapped
+// advance of the Gunrock page, step 3). A warp reserves the output slots of
+// its 32 rows with one atomic add on the next level's length (the edge bits
+// of nxt->qpack); every entry of a row writes its slot of pad[(k + 1) & 1],
+// the claimed neighbour or -1.
+template <typename RowT>
+__device__ void push_padded(const Params<RowT>& p, int k, unsigned long long L, LevelSlot* nxt,
+                            Tally& t, bool pre)
+{
+    const int32_t* in = p.pad[k & 1];
+    int32_t* out = p.pad[(k + 1) & 1];
+    const int lane = threadIdx.x & 31;
+    const unsigned long long stride = (unsigned long long)gridDim.x * blockDim.x;
+    const unsigned long long emask = (1ull << p.eb) - 1ull;
+    for (unsigned long long i0 = (unsigned long long)blockIdx.x * blockDim.x + (threadIdx.x & ~31u);
+         i0 < L; i0 += stride) {
+        const unsigned long long i = i0 + lane;
+        const int32_t v = i < L ? ldcg(in + i) : -1;
+        RowT b = 0, deg = 0;
+        if (v >= 0) {
+            b = p.row_ptr[v];
+            deg = p.row_ptr[v + 1] - b;
+        }
+        const unsigned long long d = (unsigned long long)deg;
+        const unsigned long long inc = warp_inclusive_scan(d);
+        const unsigned long long tot = __shfl_sync(kFull, inc, 31);
+        unsigned long long base = 0ull;
+        if (lane == 31 && tot != 0ull)
+            base = atomicAdd(&nxt->qpack, tot) & emask;
+        base = __shfl_sync(kFull, base, 31) + inc - d;
+        for (RowT j = 0; j < deg; ++j) {
+            const int32_t w = p.col[b + j];
+            const bool won = claim(p, k, w, v, pre);
+            out[base + (unsigned long long)j] = won ? w : -1;
+            if (won) {
+                const RowT wd = p.row_ptr[w + 1] - p.row_ptr[w];
+                t.found += 1;
+                t.edges += (unsigned long long)wd;
+                t.maxdeg = (unsigned long long)wd > t.maxdeg ? (unsigned long long)wd : t.maxdeg;
+            }
+        }
+    }
+}
+
 // ------------------------------------------------------------ S7 pull level
 
-constexpr int kHeadVerts = 4;    // head probes per lane in flight
+constexpr int kHeadVerts = 4;    // probe tests per lane in flight
 constexpr int kPullVerts = 2;    // miss rows per lane in flight
 constexpr int kPullRounds = 6;   // two-entry probe rounds before the warp takes a row
 constexpr int kPullList = 1024;  // per-warp list of unvisited vertices
@@ -864,10 +1043,10 @@ constexpr int kPullWin = 128;    // visited-bitmap words per warp window (4,096 
 // 32 words.
 //
 // A list pass (pull_list) first tests, for every entry, the probe neighbour
-// stored in the head array (read nearly sequentially, with the degree;
-// kHeadVerts entries per lane in flight, so their head -> frontier-bitmap
-// chains overlap); most rows found by a wide pull level resolve there and
-// never touch row_ptr or col. Rows that miss are scanned in CSR order, two
+// stored in the probe array (read nearly sequentially, with the flag that
+// marks a one-entry row; kHeadVerts entries per lane in flight, so their
+// probe -> frontier-bitmap chains overlap); most rows found by a wide pull
+// level resolve there, never touch row_ptr or col, and need no parent store. Rows that miss are scanned in CSR order, two
 // entries per round and kPullVerts rows per lane; one still unresolved after
 // kPullRounds rounds is scanned by the whole warp, 32 entries per step, and
 // the lowest hitting lane gives the first frontier neighbour in CSR order, as
@@ -877,22 +1056,60 @@ constexpr int kPullWin = 128;    // visited-bitmap words per warp window (4,096 
 // atomics are needed, and every next-frontier word is written, so that bitmap
 // needs no clearing.
 
+// x is found at level k with parent par. A parent that is x's probe
+// neighbour is only flagged in the hop code (the end-of-search pass writes
+// it); any other parent is stored now.
 template <typename RowT>
 __device__ __forceinline__ void pull_resolve(const Params<RowT>& p, int k, Tally& t,
                                              uint32_t* wfound, int w0, int32_t x, int32_t par,
-                                             int32_t deg)
+                                             bool par_is_probe)
 {
-    record_dist(p, x, k + 1);
-    if (p.parent != nullptr)
+    const bool flag = par_is_probe && p.defer_parent;
+    record_dist(p, x, k + 1, flag);
+    if (p.parent != nullptr && !flag)
         p.parent[x] = par;
     atomicOr(&wfound[(x >> 5) - w0], 1u << (x & 31));
     t.found += 1;
-    t.edges += (unsigned long long)deg;
-    t.maxdeg = (unsigned long long)deg > t.maxdeg ? (unsigned long long)deg : t.maxdeg;
+}
+
+// Warp-collective: the lanes with `found` append their vertex to the queue
+// of F_{k+1} (slot nxt, queue (k + 1) & 1) with one packed atomic for the
+// warp; slot order and degree-prefix order agree as in the CTA stage.
+template <typename RowT>
+__device__ __forceinline__ void emit_found(const Params<RowT>& p, int k, LevelSlot* nxt,
+                                           int32_t v, bool found)
+{
+    if (__ballot_sync(kFull, found) == 0u)
+        return;
+    const int lane = threadIdx.x & 31;
+    RowT b = 0, deg = 0;
+    if (found) {
+        b = p.row_ptr[v];
+        deg = p.row_ptr[v + 1] - b;
+    }
+    const bool take = found && deg > 0;
+    const unsigned tm = __ballot_sync(kFull, take);
+    const unsigned long long d = take ? (unsigned long long)deg : 0ull;
+    const unsigned long long inc = warp_inclusive_scan(d);
+    const unsigned long long tot = __shfl_sync(kFull, inc, 31);
+    const unsigned long long md = warp_max(d);
+    unsigned long long old = 0ull;
+    if (lane == 0 && tm != 0u) {
+        old = atomicAdd(&nxt->qpack, ((unsigned long long)__popc(tm) << p.eb) | tot);
+        atomicMax(&nxt->maxdeg, md);
+    }
+    old = __shfl_sync(kFull, old, 0);
+    if (take) {
+        const int qs = (k + 1) & 1;
+        const unsigned long long slot = (old >> p.eb) + __popc(tm & ((1u << lane) - 1u));
+        p.qv[qs][slot] = v;
+        p.qbeg[qs][slot] = b;
+        p.qoff[qs][slot] = (RowT)((old & ((1ull << p.eb) - 1ull)) + inc - d);
+    }
 }
 
 // One pass over the warp's list wlist[0, total) of unvisited vertices, all in
-// the window whose first visited-bitmap word is w0: phase 1 (head probes)
+// the window whose first visited-bitmap word is w0: phase 1 (probe tests)
 // then phase 2 (row scans of the misses). Found vertices get their bit in
 // wfound (indexed by word - w0).
 template <typename RowT>
@@ -902,31 +1119,37 @@ __device__ void pull_list(const Params<RowT>& p, int k, Tally& t, int32_t* wlist
     const uint32_t* fcur = p.fb[k & 1];
     const int lane = threadIdx.x & 31;
     // Phase 1: every list entry's probe neighbour, kHeadVerts per lane in
-    // flight. Hits resolve here; a miss with more than one edge is
-    // written back to the front of the list (never past an entry already
-    // read), so phase 2 scans rows for misses only and no lane of a
-    // round idles behind a hit.
+    // flight. Hits resolve here. A miss whose row is that one neighbour is
+    // not found at this level (its one edge counts toward the unvisited
+    // edges); any other miss is written back to the front of the list
+    // (never past an entry already read), so phase 2 scans rows for those
+    // misses only and no lane of a round idles behind a hit.
     int nmiss = 0;
     for (int base = 0; base < total; base += 32 * kHeadVerts) {
         int32_t hv[kHeadVerts];
-        int2 hd[kHeadVerts];
+        uint32_t hc[kHeadVerts];
         uint32_t hf[kHeadVerts];
 #pragma unroll
         for (int b = 0; b < kHeadVerts; ++b) {
             const int j = base + b * 32 + lane;
             hv[b] = j < total ? wlist[j] : -1;
-            hd[b] = hv[b] >= 0 ? __ldg(p.head + hv[b]) : make_int2(-1, 0);
+            hc[b] = hv[b] >= 0 ? __ldg(p.probe + hv[b]) : kProbeNone;
         }
 #pragma unroll
-        for (int b = 0; b < kHeadVerts; ++b)
-            hf[b] = hd[b].x >= 0 ? ldcg(fcur + (hd[b].x >> 5)) : 0u;
+        for (int b = 0; b < kHeadVerts; ++b) {
+            const uint32_t u = hc[b] & kProbeNone;
+            hf[b] = u != kProbeNone ? ldcg(fcur + (u >> 5)) : 0u;
+        }
         __syncwarp();
 #pragma unroll
         for (int b = 0; b < kHeadVerts; ++b) {
-            const bool hit = hd[b].x >= 0 && ((hf[b] >> (hd[b].x & 31)) & 1u);
+            const uint32_t u = hc[b] & kProbeNone;
+            const bool hit = u != kProbeNone && ((hf[b] >> (u & 31)) & 1u);
             if (hit)
-                pull_resolve(p, k, t, wfound, w0, hv[b], hd[b].x, hd[b].y);
-            const bool miss = hv[b] >= 0 && !hit && hd[b].y > 1;
+                pull_resolve(p, k, t, wfound, w0, hv[b], (int32_t)u, true);
+            else if (hv[b] >= 0 && (hc[b] >> 31))
+                t.edges += 1ull;  // the only edge leads outside F_k
+            const bool miss = hv[b] >= 0 && !hit && u != kProbeNone && !(hc[b] >> 31);
             const unsigned mm = __ballot_sync(kFull, miss);
             if (miss)
                 wlist[nmiss + __popc(mm & ((1u << lane) - 1u))] = hv[b];
@@ -1021,15 +1244,18 @@ __device__ void pull_list(const Params<RowT>& p, int k, Tally& t, int32_t* wlist
             }
         }
 #pragma unroll
-        for (int b = 0; b < kPullVerts; ++b)
+        for (int b = 0; b < kPullVerts; ++b) {
             if (par[b] >= 0)
-                pull_resolve(p, k, t, wfound, w0, v[b], par[b], deg[b]);
+                pull_resolve(p, k, t, wfound, w0, v[b], par[b], false);
+            else if (v[b] >= 0)
+                t.edges += (unsigned long long)deg[b];  // stays unvisited
+        }
     }
 }
 
 template <typename RowT>
 __device__ void pull_level(const Params<RowT>& p, int k, Tally& t, int32_t* wlist,
-                           uint32_t* wfound, uint32_t* wvis)
+                           uint32_t* wfound, uint32_t* wvis, LevelSlot* emit)
 {
     uint32_t* fnext = p.fb[(k + 1) & 1];
     const int lane = threadIdx.x & 31;
@@ -1080,6 +1306,20 @@ __device__ void pull_level(const Params<RowT>& p, int k, Tally& t, int32_t* wlis
             if (j >= kPullWin / 32)
                 break;
         }
+        // Few unvisited vertices at the level's start: the window's finds also
+        // go to the next queue, a warp's worth of vertices per step.
+        if (emit != nullptr) {
+            for (int jj = 0; jj < kPullWin / 32; ++jj) {
+                const int i = 32 * jj + lane;
+                uint32_t f = i < nwin ? wfound[i] : 0u;
+                while (__any_sync(kFull, f != 0u)) {
+                    const bool has = f != 0u;
+                    const int bit = has ? __ffs(f) - 1 : 0;
+                    f &= f - 1u;
+                    emit_found(p, k, emit, ((a + i) << 5) + bit, has);
+                }
+            }
+        }
 #pragma unroll
         for (int jj = 0; jj < kPullWin / 32; ++jj) {
             const int i = 32 * jj + lane;
@@ -1120,11 +1360,14 @@ __device__ void queue_to_bitmap_set(const Params<RowT>& p, int k, int qn)
 }
 
 // F_k from bitmap to queue (with row starts and the degree prefix), through
-// the same stage as push levels; counts go to the current slot's qpack.
+// the same stage as push levels; counts go to the current slot's qpack, and
+// the largest degree of F_k (which a pull level does not count) to its
+// maxdeg.
 template <typename RowT>
 __device__ void bitmap_to_queue(const Params<RowT>& p, int k, const Smem<RowT>& sm,
                                 SmemScalars& ss, LevelSlot* cur)
 {
+    unsigned long long md = 0ull;
     constexpr int kBatch = 4;  // bitmap words per thread loaded together
     const uint32_t* f = p.fb[k & 1];
     const int sel = k & 1;
@@ -1147,6 +1390,7 @@ __device__ void bitmap_to_queue(const Params<RowT>& p, int k, const Smem<RowT>& 
                 const int32_t v = (w << 5) + bit;
                 const RowT rb = p.row_ptr[v];
                 const RowT deg = p.row_ptr[v + 1] - rb;
+                md = (unsigned long long)deg > md ? (unsigned long long)deg : md;
                 stage_push(p, sm, ss, cur, sel, v, rb, deg, deg > 0);
             }
         }
@@ -1154,6 +1398,9 @@ __device__ void bitmap_to_queue(const Params<RowT>& p, int k, const Smem<RowT>& 
             stage_flush(p, sm, ss, cur, sel);
     }
     stage_flush(p, sm, ss, cur, sel);
+    md = warp_max(md);
+    if ((threadIdx.x & 31) == 0 && md != 0ull)
+        atomicMax(&cur->maxdeg, md);
 }
 
 // S2: the direction of level k. Only symmetric graphs may pull. In AUTO
@@ -1168,7 +1415,8 @@ template <typename RowT>
 __device__ __forceinline__ int choose_direction(const Params<RowT>& p, int prev_dir, long long F,
                                                 long long mF, long long mU, long long nonisolated)
 {
-    if (!p.symmetric || p.direction == BFS_CSR_DIR_PUSH)
+    if (!p.symmetric || p.direction == BFS_CSR_DIR_PUSH ||
+        p.frontier_output == BFS_CSR_FRONTIER_PADDED)
         return BFS_CSR_DIR_PUSH;
     if (p.direction == BFS_CSR_DIR_PULL)
         return BFS_CSR_DIR_PULL;
@@ -1225,51 +1473,54 @@ __device__ void solo_levels(const Params<RowT>& p, int k, int qn, RowT qm, long 
     for (;;) {
         const unsigned long long t0 = tid == 0 ? global_timer_ns() : 0ull;
         const RowT M = co[qn];
-        // expand: at most kItems edges per thread, loads batched
-        int32_t vv[kItems], uu[kItems];
+        // expand in rounds of kItems edges per thread, the loads of a round
+        // batched; M is at most the stage capacity, so every winner fits it
+        unsigned long long f_loc = 0ull, e_loc = 0ull, m_loc = 0ull;
+        for (RowT r0 = 0; r0 < M; r0 += (RowT)(kItems * bd)) {
+            int32_t vv[kItems], uu[kItems];
 #pragma unroll
-        for (int it = 0; it < kItems; ++it) {
-            const RowT e = (RowT)(it * bd + tid);
-            vv[it] = -1;
-            uu[it] = 0;
-            if (e < M) {
-                int lo = 0, hi = qn;
-                while (hi - lo > 1) {
-                    const int mid = (lo + hi) >> 1;
-                    if (co[mid] <= e)
-                        lo = mid;
-                    else
-                        hi = mid;
+            for (int it = 0; it < kItems; ++it) {
+                const RowT e = r0 + (RowT)(it * bd + tid);
+                vv[it] = -1;
+                uu[it] = 0;
+                if (e < M) {
+                    int lo = 0, hi = qn;
+                    while (hi - lo > 1) {
+                        const int mid = (lo + hi) >> 1;
+                        if (co[mid] <= e)
+                            lo = mid;
+                        else
+                            hi = mid;
+                    }
+                    uu[it] = cv[lo];
+                    vv[it] = p.col[cb[lo] + (e - co[lo])];
                 }
-                uu[it] = cv[lo];
-                vv[it] = p.col[cb[lo] + (e - co[lo])];
             }
-        }
-        bool won[kItems];
-        claim_batch(p, j, vv, uu, false, won);
-        RowT wb[kItems], we[kItems];
+            bool won[kItems];
+            claim_batch(p, j, vv, uu, false, won);
+            RowT wb[kItems], we[kItems];
 #pragma unroll
-        for (int it = 0; it < kItems; ++it) {
-            wb[it] = 0;
-            we[it] = 0;
-            if (won[it]) {
-                wb[it] = p.row_ptr[vv[it]];
-                we[it] = p.row_ptr[vv[it] + 1];
+            for (int it = 0; it < kItems; ++it) {
+                wb[it] = 0;
+                we[it] = 0;
+                if (won[it]) {
+                    wb[it] = p.row_ptr[vv[it]];
+                    we[it] = p.row_ptr[vv[it] + 1];
+                }
+            }
+#pragma unroll
+            for (int it = 0; it < kItems; ++it) {
+                const RowT deg = we[it] - wb[it];
+                if (won[it]) {
+                    f_loc += 1ull;
+                    e_loc += (unsigned long long)deg;
+                    m_loc = (unsigned long long)deg > m_loc ? (unsigned long long)deg : m_loc;
+                }
+                stage_push(p, sm, ss, nullptr, 0, vv[it], wb[it], deg, won[it] && deg > 0);
             }
         }
         // Tallies per warp, then one shared atomic per warp and counter; the
         // level has at most one stage of winners, so no slot overflows.
-        unsigned long long f_loc = 0ull, e_loc = 0ull, m_loc = 0ull;
-#pragma unroll
-        for (int it = 0; it < kItems; ++it) {
-            const RowT deg = we[it] - wb[it];
-            if (won[it]) {
-                f_loc += 1ull;
-                e_loc += (unsigned long long)deg;
-                m_loc = (unsigned long long)deg > m_loc ? (unsigned long long)deg : m_loc;
-            }
-            stage_push(p, sm, ss, nullptr, 0, vv[it], wb[it], deg, won[it] && deg > 0);
-        }
         f_loc = warp_sum(f_loc);
         e_loc = warp_sum(e_loc);
         m_loc = warp_max(m_loc);
@@ -1300,7 +1551,7 @@ __device__ void solo_levels(const Params<RowT>& p, int k, int qn, RowT qm, long 
         const long long Un = Uj - Fn;   // unvisited at level j + 1's start
         const long long mUn = mUj - (long long)en;
         bool stop = Fn == 0 || (p.max_depth >= 0 && j + 1 >= p.max_depth) ||
-                    (long long)en > (long long)p.narrow_max || nq > sm.cap ||
+                    (long long)en > (long long)p.narrow_max || nq >= sm.wcap ||
                     j + 1 - k >= kSoloMaxLevels;
         if (!stop && choose_direction(p, BFS_CSR_DIR_PUSH, Fn, (long long)en, mUn, nonisolated) !=
                          BFS_CSR_DIR_PUSH)
@@ -1387,19 +1638,32 @@ __device__ void solo_levels(const Params<RowT>& p, int k, int qn, RowT qm, long 
 
 // ------------------------------------------------------------ S10 output
 
-// dist from the hop codes, once the search has ended. A warp converts 1,024
-// consecutive vertices per step: lane l reads the 4 codes of vertices
-// base + 128 q + 4 l (q = 0..7) as one word each and writes their distances
-// as one 16-byte store each, so every store instruction of the warp covers
-// 512 contiguous bytes and all eight code loads are in flight together.
-// Codes of kHopFar keep the distance their discovery wrote to dist.
+// dist and parent from the hop codes, once the search has ended. A warp
+// converts 1,024 consecutive vertices per step: lane l reads the 4 codes of
+// vertices base + 128 q + 4 l (q = 0..7) as one word each and writes their
+// distances and parents as one 16-byte store each, so every store
+// instruction of the warp covers 512 contiguous bytes and all eight code
+// loads are in flight together. With defer_parent the parents are written
+// the same way: those of flagged codes come from probe[] (four at a time,
+// 16-byte loads), a reached vertex without the flag kept the parent its
+// discovery stored, an unreached one gets -1. Codes of kHopFar keep the
+// distance their discovery wrote to dist.
 __device__ __forceinline__ int32_t hop_to_dist(uint32_t c, const int32_t* dist, int64_t v)
 {
-    return c == 0u ? -1 : (c == kHopFar ? ldcg(dist + v) : (int32_t)c - 1);
+    const uint32_t d = c & 0x7fu;
+    return d == 0u ? -1 : (d == kHopFar ? ldcg(dist + v) : (int32_t)d - 1);
+}
+
+__device__ __forceinline__ int32_t hop_to_parent(uint32_t c, uint32_t probe, const int32_t* parent,
+                                                 int64_t v)
+{
+    if ((c & 0x7fu) == 0u)
+        return -1;
+    return (c & kHopProbe) ? (int32_t)(probe & kProbeNone) : ldcg(parent + v);
 }
 
 template <typename RowT>
-__device__ void write_dist(const Params<RowT>& p)
+__device__ void write_outputs(const Params<RowT>& p)
 {
     constexpr int kQ = 8;
     const int64_t n = p.n;
@@ -1407,7 +1671,8 @@ __device__ void write_dist(const Params<RowT>& p)
     const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
     const uint32_t* h4 = reinterpret_cast<const uint32_t*>(p.hop);  // 16-byte aligned
-    const bool vec = (reinterpret_cast<uintptr_t>(p.dist) & 15u) == 0;
+    const bool vec = p.vec_out != 0;
+    const bool par = p.parent != nullptr && p.defer_parent;
     const int64_t nfull = vec ? n / (128 * kQ) : 0;   // steps with every vertex < n
     for (int64_t st = gw; st < nfull; st += nw) {
         const int64_t base = st * 128 * kQ;
@@ -1425,13 +1690,36 @@ __device__ void write_dist(const Params<RowT>& p)
             o.w = hop_to_dist(c[q] >> 24, p.dist, v + 3);
             *reinterpret_cast<int4*>(p.dist + v) = o;
         }
+        if (par) {
+            uint4 pr[kQ];
+#pragma unroll
+            for (int q = 0; q < kQ; ++q) {
+                const int64_t v = base + 128 * q + 4 * lane;
+                pr[q] = (c[q] & 0x80808080u) ? __ldg(reinterpret_cast<const uint4*>(p.probe + v))
+                                             : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int q = 0; q < kQ; ++q) {
+                const int64_t v = base + 128 * q + 4 * lane;
+                int4 o;
+                o.x = hop_to_parent(c[q] & 0xffu, pr[q].x, p.parent, v);
+                o.y = hop_to_parent((c[q] >> 8) & 0xffu, pr[q].y, p.parent, v + 1);
+                o.z = hop_to_parent((c[q] >> 16) & 0xffu, pr[q].z, p.parent, v + 2);
+                o.w = hop_to_parent(c[q] >> 24, pr[q].w, p.parent, v + 3);
+                *reinterpret_cast<int4*>(p.parent + v) = o;
+            }
+        }
     }
-    // The rest (or everything when dist is not 16-byte aligned), one vertex
-    // per thread.
+    // The rest (or everything when the outputs are not 16-byte aligned), one
+    // vertex per thread.
     const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t v = nfull * 128 * kQ + tid; v < n; v += stride)
-        p.dist[v] = hop_to_dist(ldcg(p.hop + v), p.dist, v);
+    for (int64_t v = nfull * 128 * kQ + tid; v < n; v += stride) {
+        const uint32_t c = ldcg(p.hop + v);
+        p.dist[v] = hop_to_dist(c, p.dist, v);
+        if (par)
+            p.parent[v] = hop_to_parent(c, (c & kHopProbe) ? __ldg(p.probe + v) : 0u, p.parent, v);
+    }
 }
 
 // ------------------------------------------------------------ kernels
@@ -1445,10 +1733,9 @@ template <typename RowT>
 __device__ __forceinline__ Smem<RowT> carve_smem(unsigned char* raw, int bd)
 {
     Smem<RowT> sm;
-    const int tile = bd * kItems;
     unsigned char* q = raw;
-    sm.cap = tile;
-    sm.wcap = tile + 1;
+    sm.cap = stage_cap<RowT>(bd);
+    sm.wcap = window_cap(bd) + 1;
     sm.sb = reinterpret_cast<RowT*>(q); q += sizeof(RowT) * sm.cap;
     sm.sd = reinterpret_cast<int32_t*>(q); q += sizeof(int32_t) * sm.cap;
     sm.sv = reinterpret_cast<int32_t*>(q); q += sizeof(int32_t) * sm.cap;
@@ -1465,8 +1752,8 @@ __device__ __forceinline__ Smem<RowT> carve_smem(unsigned char* raw, int bd)
 template <typename RowT>
 __host__ __device__ inline size_t level_smem_bytes(int bd)
 {
-    const size_t tile = (size_t)bd * kItems;
-    const size_t push = (sizeof(RowT) + 8) * tile + (2 * sizeof(RowT) + 4) * (tile + 1) + 16;
+    const size_t scap = (size_t)stage_cap<RowT>(bd), wcap = (size_t)window_cap(bd);
+    const size_t push = (sizeof(RowT) + 8) * scap + (2 * sizeof(RowT) + 4) * (wcap + 1) + 16;
     const size_t pull = (size_t)(bd / 32) * (kPullList + 2 * kPullWin) * sizeof(uint32_t);
     const size_t wstage = (size_t)(bd / 32) * kWarpStage * (sizeof(RowT) + 8);
     const size_t m = push > pull ? push : pull;
@@ -1514,6 +1801,10 @@ __global__ void __launch_bounds__(512, 2) level_kernel(Params<RowT> p)
             break;
         }
         const long long F = (long long)found;
+        // m_F: counted directly by a push level; after a pull level, the
+        // unvisited edges at its start minus those it left unvisited.
+        const long long mF = prev_dir == BFS_CSR_DIR_PULL ? ueprev + (long long)fedges
+                                                          : (long long)fedges;
         if (F == 0 || (p.max_depth >= 0 && k >= p.max_depth)) {
             if (leader) {
                 const int nl = F == 0 ? k : k + 1;
@@ -1526,7 +1817,7 @@ __global__ void __launch_bounds__(512, 2) level_kernel(Params<RowT> p)
                     st.advance = 0;
                     st.reserved = 0;
                     st.frontier = F;
-                    st.frontier_edges = (long long)fedges;
+                    st.frontier_edges = mF;
                     st.unvisited = uprev - F;
                     st.max_degree = (long long)maxdeg;
                     st.t_start_ns = (long long)t_end;
@@ -1546,21 +1837,21 @@ __global__ void __launch_bounds__(512, 2) level_kernel(Params<RowT> p)
         if (budget <= 0)
             break;
         const unsigned long long t_level = leader ? global_timer_ns() : 0ull;
-        const long long mF = (long long)fedges;
         const long long U = uprev - F;
         const long long mU = ueprev - mF;
         const int dir = choose_direction(p, prev_dir, F, mF, mU, nonisolated);
         Tally t = {0ull, 0ull, 0ull};
         int adv = 0;
+        unsigned long long md = maxdeg;  // largest degree in F_k (known to push levels)
 
         // Narrow push level: CTA 0 runs it (and the following narrow ones)
         // alone; everyone meets at the barrier and resumes where it stopped.
         if (dir == BFS_CSR_DIR_PUSH && prev_dir != BFS_CSR_DIR_PULL && p.narrow_max > 0 &&
-            p.level_budget == INT_MAX) {
+            p.level_budget == INT_MAX && p.frontier_output == BFS_CSR_FRONTIER_COMPACT) {
             const unsigned long long qp0 = ldcg_u64(&cur->qpack);
             const int qn0 = (int)(qp0 >> p.eb);
             const long long qm0 = (long long)(qp0 & ((1ull << p.eb) - 1ull));
-            if (qm0 <= (long long)p.narrow_max && qn0 <= sm.cap) {
+            if (qm0 <= (long long)p.narrow_max && qn0 < sm.wcap) {
                 if (blockIdx.x == 0)
                     solo_levels(p, k, qn0, (RowT)qm0, F, U, mU, maxdeg, sm, ss, target,
                                 nonisolated);
@@ -1592,22 +1883,31 @@ __global__ void __launch_bounds__(512, 2) level_kernel(Params<RowT> p)
                 int32_t* wlist = reinterpret_cast<int32_t*>(smem_raw) + wid * kPullList;
                 uint32_t* wfound = reinterpret_cast<uint32_t*>(smem_raw) +
                                    (blockDim.x >> 5) * kPullList + wid * 2 * kPullWin;
-                pull_level(p, k, t, wlist, wfound, wfound + kPullWin);
+                pull_level(p, k, t, wlist, wfound, wfound + kPullWin,
+                           U <= p.emit_max ? nxt : nullptr);
             }
         } else {
-            if (prev_dir == BFS_CSR_DIR_PULL) {
+            // After a pull level that started with few unvisited vertices
+            // (uprev is that count) the queue of F_k was built as it found
+            // them; otherwise it is built from the frontier bitmap now.
+            if (prev_dir == BFS_CSR_DIR_PULL && uprev > p.emit_max) {
                 bitmap_to_queue(p, k, sm, ss, cur);
                 if (!grid_barrier(p, target)) break;
+                md = ldcg_u64(&cur->maxdeg);
             }
             const unsigned long long qp = ldcg_u64(&cur->qpack);
             const int qn = (int)(qp >> p.eb);
             const RowT qm = (RowT)(qp & ((1ull << p.eb) - 1ull));
-            if (p.advance == BFS_CSR_ADV_BINNED)
+            if (p.frontier_output == BFS_CSR_FRONTIER_PADDED)
+                adv = BFS_CSR_ADV_PADDED;
+            else if (p.frontier_output == BFS_CSR_FRONTIER_PADDED_FILTER)
+                adv = BFS_CSR_ADV_MERGE_PATH;
+            else if (p.advance == BFS_CSR_ADV_BINNED)
                 adv = BFS_CSR_ADV_BINNED;
             else if (p.advance == BFS_CSR_ADV_MERGE_PATH)
                 adv = BFS_CSR_ADV_MERGE_PATH;
             else
-                adv = (qn >= p.mp_min_frontier || maxdeg >= (unsigned long long)p.binned_max_deg)
+                adv = (qn >= p.mp_min_frontier || md >= (unsigned long long)p.binned_max_deg)
                           ? BFS_CSR_ADV_MERGE_PATH : BFS_CSR_ADV_BINNED;
             if (leader) {
                 LevelSlot* z = &p.ctl->slot[(k + 2) & 3];
@@ -1622,10 +1922,20 @@ __global__ void __launch_bounds__(512, 2) level_kernel(Params<RowT> p)
             // when most targets are already visited (late, wide levels) and
             // costs a round trip otherwise.
             const bool pre = (long long)qm >= 65536 && 2 * U < nonisolated;
-            if (adv == BFS_CSR_ADV_MERGE_PATH)
+            if (adv == BFS_CSR_ADV_PADDED) {
+                // qm is the length of the padded frontier here
+                push_padded(p, k, qp & ((1ull << p.eb) - 1ull), nxt, t, pre);
+            } else if (adv == BFS_CSR_ADV_MERGE_PATH) {
                 push_warp_mp(p, k, qn, qm, smem_raw, nxt, t, pre);
-            else
+                if (p.frontier_output == BFS_CSR_FRONTIER_PADDED_FILTER) {
+                    // every slot of the padded output is written before the
+                    // filter reads it
+                    if (!grid_barrier(p, target)) break;
+                    filter_padded(p, (unsigned long long)qm, sm, ss, nxt, (k + 1) & 1, t);
+                }
+            } else {
                 push_binned(p, k, qn, qm, sm, ss, nxt, t, pre);
+            }
         }
         // The level's record. Every CTA stamps the end of its share of the
         // work (the latest stamp wins); the next level's stamp is cleared
@@ -1642,12 +1952,12 @@ __global__ void __launch_bounds__(512, 2) level_kernel(Params<RowT> p)
             st->frontier = F;
             st->frontier_edges = mF;
             st->unvisited = U;
-            st->max_degree = (long long)maxdeg;
+            st->max_degree = (long long)md;
             st->t_start_ns = (long long)t_level;
             if (k + 1 < p.stats_cap)
                 p.stats[k + 1].t_work_ns = 0;
         }
-        publish_tally<RowT>(t, nxt, ss);
+        publish_tally<RowT>(t, nxt, ss, dir == BFS_CSR_DIR_PULL);
         if (!grid_barrier(p, target)) break;
         ++k;
         --budget;
@@ -1656,7 +1966,7 @@ __global__ void __launch_bounds__(512, 2) level_kernel(Params<RowT> p)
     // S10: every CTA saw the same empty (or depth-bounded) frontier after
     // the last grid barrier, so all hop codes are final.
     if (finished && p.defer_dist)
-        write_dist(p);
+        write_outputs(p);
 
     // Leave: the last CTA out resets the barrier for the next launch.
     __syncthreads();
@@ -1670,17 +1980,31 @@ __global__ void __launch_bounds__(512, 2) level_kernel(Params<RowT> p)
                 p.stamps[2] = (long long)global_timer_ns();
             p.ctl->bar = 0ull;
             p.ctl->exit_count = 0u;
+            if (p.graph_cond != 0ull) {
+                // The graph's while loop runs another launch until the search
+                // has ended or failed. Every launch either runs a level or
+                // ends the search, so more than n + 1 launches would mean a
+                // fault: it ends the loop with an error instead of spinning.
+                bool stop = ldcg(&p.ctl->done) != 0 || ldcg(&p.ctl->status) != BFS_CSR_OK;
+                if (!stop && (long long)ldcg(&p.ctl->level) > (long long)p.n + 1) {
+                    atomicCAS(&p.ctl->status, BFS_CSR_OK, BFS_CSR_EDEVICE);
+                    stop = true;
+                }
+                if (stop)
+                    cudaGraphSetConditional(p.graph_cond, 0u);
+            }
             __threadfence();
         }
     }
 }
 
-// S1: reset the run state and seed the source. parent is filled with -1
-// (source: itself); with bitmap discovery the hop codes are cleared (source:
-// distance 0) and dist is left to the end of the search, otherwise dist is
-// filled with -1 (source: 0). visited starts as the dead bitmap (vertices of
-// degree 0 and padding bits beyond n) plus the source bit, and slot 0 holds
-// F_0 = {source}.
+// S1: reset the run state and seed the source. With bitmap discovery the hop
+// codes are cleared (source: distance 0) and dist is left to the end of the
+// search; so is parent when defer_parent is set (then only parent[source] =
+// source is stored). Whatever is not deferred is filled with -1 here (the
+// source: distance 0, parent itself).
+// visited starts as the dead bitmap (vertices of degree 0 and padding bits
+// beyond n) plus the source bit, and slot 0 holds F_0 = {source}.
 template <typename RowT>
 __global__ void init_kernel(Params<RowT> p, const uint32_t* __restrict__ dead, int32_t source,
                             int use_dead)
@@ -1688,10 +2012,13 @@ __global__ void init_kernel(Params<RowT> p, const uint32_t* __restrict__ dead, i
     const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     const int32_t n = p.n;
-    const bool wdist = !p.defer_dist;
+    const bool fill = !p.defer_dist;
+    const bool fill_parent = !p.defer_parent;
     if (p.stamps != nullptr && tid == 0)
         p.stamps[0] = (long long)global_timer_ns();
-    int32_t* outs[2] = {wdist ? p.dist : nullptr, p.parent};
+    if (!fill_parent && p.parent != nullptr && tid == 0)
+        p.parent[source] = source;
+    int32_t* outs[2] = {fill ? p.dist : nullptr, fill_parent ? p.parent : nullptr};
     const int32_t seed[2] = {0, source};
     for (int o = 0; o < 2; ++o) {
         int32_t* a = outs[o];
@@ -1759,7 +2086,11 @@ __global__ void init_kernel(Params<RowT> p, const uint32_t* __restrict__ dead, i
         c->slot[0].found = 1ull;
         c->slot[0].fedges = (unsigned long long)deg;
         c->slot[0].maxdeg = (unsigned long long)deg;
-        if (deg > 0) {
+        if (p.frontier_output == BFS_CSR_FRONTIER_PADDED) {
+            // F_0 as a padded frontier of one slot
+            p.pad[0][0] = source;
+            c->slot[0].qpack = 1ull;
+        } else if (deg > 0) {
             c->slot[0].qpack = (1ull << p.eb) | (unsigned long long)deg;
             p.qv[0][0] = source;
             p.qbeg[0][0] = b;
@@ -1821,21 +2152,22 @@ __global__ void dead_kernel(const RowT* __restrict__ row_ptr, int32_t n, int32_t
         atomicAdd(reinterpret_cast<unsigned long long*>(nonisolated), (unsigned long long)live);
 }
 
-// Per-vertex head of the row: (a probe neighbour or -1, degree), 8 bytes, so
-// that a pull level tests one likely parent of each unvisited vertex from a
-// nearly sequential array instead of a row_ptr entry and a random col block.
-// The probe neighbour is the one of highest degree among the first
-// kHeadScan entries of the row (the earliest on ties). High-degree vertices
-// are reached first in a search from almost any source, so for a vertex
-// found by a pull level that neighbour is usually in the current frontier;
-// on R-MAT inputs the first neighbour in CSR order, the plain choice, is
-// there for only about a third of them. Derived from the CSR at create time;
-// the rows themselves are never copied.
+// Per vertex, its probe neighbour: the one of highest degree among the
+// row's first kHeadScan entries (the earliest on ties), with bit 31 set when
+// it is the row's only entry, kProbeNone for an empty row. A pull level
+// tests this one likely parent of each unvisited vertex first, from a
+// sequential 4-byte array instead of a row_ptr entry and a random col
+// block: high-degree vertices are reached first in a search from almost any
+// source, so for a vertex a pull level finds that neighbour is nearly always
+// in the current frontier (on R-MAT inputs the first neighbour in CSR
+// order, the plain choice, is there for only about a third of them). A
+// vertex found through its probe needs no parent store (its hop code is
+// flagged). Derived from the CSR at create time; rows are never copied.
 constexpr int kHeadScan = 64;
 
 template <typename RowT>
-__global__ void head_kernel(const RowT* __restrict__ row_ptr, const int32_t* __restrict__ col,
-                            int32_t n, int2* head)
+__global__ void probe_kernel(const RowT* __restrict__ row_ptr, const int32_t* __restrict__ col,
+                             int32_t n, uint32_t* probe)
 {
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < n; v += stride) {
@@ -1863,7 +2195,7 @@ __global__ void head_kernel(const RowT* __restrict__ row_ptr, const int32_t* __r
                 }
             }
         }
-        head[v] = make_int2(best, (int32_t)d);
+        probe[v] = d == 0 ? kProbeNone : ((uint32_t)best | (d == 1 ? 0x80000000u : 0u));
     }
 }
 

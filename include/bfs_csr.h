@@ -47,18 +47,57 @@ extern "C" {
 
 /* Load balance of a top-down (push) level. */
 #define BFS_CSR_ADV_AUTO 0      /* merge-path when |F| >= merge_path_min_frontier
-                                   or the largest frontier degree >= binned_max_degree */
+                                   or the largest frontier degree >= binned_max_degree,
+                                   else binned (the Gunrock paper's static hybrid; with
+                                   the default threshold 0 every push level takes the
+                                   merge path, measured at least as fast here) */
 #define BFS_CSR_ADV_BINNED 1    /* thread / warp / CTA per vertex by degree */
 #define BFS_CSR_ADV_MERGE_PATH 2 /* edge-balanced: degree prefix + search */
 #define BFS_CSR_ADV_SINGLE_CTA 3 /* (level records only) a narrow level run by one CTA */
+#define BFS_CSR_ADV_PADDED 4     /* (level records only) one thread per slot of a
+                                    sentinel-padded frontier, see BFS_CSR_FRONTIER_PADDED */
 
 /* How a top-down level decides who discovered a vertex. */
 #define BFS_CSR_DISC_BITMAP 0   /* atomicOr on a visited bitmap */
 #define BFS_CSR_DISC_CAS 1      /* atomicCAS on dist (-1 -> level + 1) */
+#define BFS_CSR_DISC_MIN 2      /* atomicMin on dist read as unsigned (-1 = UINT_MAX); the
+                                   claim is won when level + 1 is below the old value
+                                   ("Gunrock: advance, filter, and the ragged-frontier
+                                   problem", step 2) */
+
+/* What a push level writes for the next frontier ("Gunrock: advance, filter,
+ * and the ragged-frontier problem", step 2: the advance writes every
+ * neighbour it claims, or an invalid sentinel in its place; an optional
+ * filter removes the sentinels). */
+#define BFS_CSR_FRONTIER_COMPACT 0       /* winners go straight to the next queue
+                                            (block-aggregated compaction) */
+#define BFS_CSR_FRONTIER_PADDED_FILTER 1 /* every frontier edge writes its neighbour or -1
+                                            into an edge-indexed array (merge-path
+                                            advance); a filter pass compacts it into the
+                                            next queue. No single-CTA levels */
+#define BFS_CSR_FRONTIER_PADDED 2        /* no filter: the padded array is the next
+                                            frontier, walked one thread per slot (the
+                                            thread-mapped advance), sentinels skipped.
+                                            Push levels only, no single-CTA levels */
+
+/* Where a pull level's parents go (bitmap discovery). Almost every vertex a
+ * pull level finds has its probe neighbour (see bfs_csr_create) as parent;
+ * END_PASS only flags those in the one-byte hop code and writes every parent
+ * once, in order, when the search ends, instead of one scattered 4-byte store
+ * each (and no -1 fill at init). AUTO picks END_PASS when the parent array
+ * (4n bytes) exceeds half of the device's L2, below which scattered stores
+ * stay in the L2. */
+#define BFS_CSR_PARENT_AUTO 0
+#define BFS_CSR_PARENT_END_PASS 1
+#define BFS_CSR_PARENT_AT_DISCOVERY 2
 
 /* Where the level loop runs. */
 #define BFS_CSR_LOOP_PERSISTENT 0 /* one cooperative kernel runs every level */
 #define BFS_CSR_LOOP_HOST 1       /* one launch plus one device->host read per level */
+#define BFS_CSR_LOOP_GRAPH 2      /* one CUDA graph launch per search: a while node, driven
+                                     from the device, whose body launches one level; the
+                                     host loop without its per-level round trip (PMPP ch. 15
+                                     notes, section 15.7, on per-level launch cost) */
 
 typedef struct bfs_csr_options {
     int32_t direction;               /* BFS_CSR_DIR_*, default AUTO */
@@ -67,7 +106,8 @@ typedef struct bfs_csr_options {
     int32_t loop_mode;               /* BFS_CSR_LOOP_*, default PERSISTENT */
     int32_t small_max_degree;        /* binned: degree < this -> thread per vertex (32) */
     int32_t cta_min_degree;          /* binned: degree >= this -> CTA per vertex (256) */
-    int32_t merge_path_min_frontier; /* auto advance threshold on |F| (4096) */
+    int32_t merge_path_min_frontier; /* auto advance threshold on |F| (0; the pages'
+                                        hybrid uses 4096) */
     int32_t binned_max_degree;       /* auto advance threshold on max degree (8192) */
     double pull_alpha;               /* auto direction after a push level: pull iff
                                         m_F * pull_alpha > m_U, the edges of the vertices
@@ -84,14 +124,20 @@ typedef struct bfs_csr_options {
                                         |F| * push_beta < vertices of nonzero degree (24);
                                         0: apply the pull_alpha rule instead */
     int32_t narrow_max_edges;        /* push levels whose frontier has at most this many
-                                        edges (and vertices) run on one CTA without
-                                        grid barriers; 0 disables; capped at the CTA's
-                                        stage (block_threads * 4); default 2048 */
+                                        edges (and vertices) run on one CTA without grid
+                                        barriers; 0 disables; capped at the CTA's stage
+                                        (block_threads * 4); default 2048 */
     int32_t lanes;                   /* searches bfs_csr_run_batch keeps in flight at once,
                                         1..8 (0 means 1); each has its own search state
                                         in the workspace and 1/lanes of the level
                                         kernel's CTAs; default 1 */
-    int32_t reserved[4];             /* zero */
+    int32_t parent_pass;             /* BFS_CSR_PARENT_*: where parents found through a
+                                        pull level's probe neighbour are written; default
+                                        AUTO */
+    int32_t frontier_output;         /* BFS_CSR_FRONTIER_*, default COMPACT; the padded
+                                        modes add two arrays of max(nnz, 1) int32 to the
+                                        workspace of each lane */
+    int32_t reserved[2];             /* zero */
 } bfs_csr_options;
 
 /* Per-level record, kept when the run completes (see bfs_csr_level_stats). */
@@ -106,7 +152,9 @@ typedef struct bfs_csr_level_stat {
     int64_t frontier;        /* |F_k| */
     int64_t frontier_edges;  /* m_F: sum of out-degrees over F_k */
     int64_t unvisited;       /* non-isolated vertices not yet reached at level start */
-    int64_t max_degree;      /* largest out-degree in F_k */
+    int64_t max_degree;      /* largest out-degree in F_k; 0 when F_k was found by
+                                a pull level and level k pulls too (a pull level
+                                does not look at the degrees of what it finds) */
     int64_t t_start_ns;      /* device global timer at the level's start */
     int64_t t_work_ns;       /* device global timer when the last CTA finished the
                                 level's work, before the barrier that ends it
@@ -135,9 +183,9 @@ int bfs_csr_workspace_bytes(int64_t n, int64_t nnz, int row_ptr_64,
  * bfs_csr_workspace_bytes, 256-byte aligned, owned by the caller. With
  * opt->validate the CSR is checked on the device; a malformed CSR gives
  * BFS_CSR_EINVAL. The call then derives, in the workspace, a bitmap of the
- * degree-0 vertices and a head array (per vertex: one probe neighbour, the
- * highest-degree one among the row's first 64 entries, and the degree) in
- * one pass over the rows. Limits: 1 <= n < 2^31, nnz < 2^31 for int32
+ * degree-0 vertices and a probe array (per vertex, 4 bytes: one probe
+ * neighbour, the highest-degree one among the row's first 64 entries, and
+ * whether it is the row's only entry) in one pass over the rows. Limits: 1 <= n < 2^31, nnz < 2^31 for int32
  * row_ptr. The call synchronises `stream`.
  */
 int bfs_csr_create(bfs_csr_handle *out, int64_t n, int64_t nnz,
@@ -214,7 +262,7 @@ int bfs_csr_level_stats(bfs_csr_handle h, bfs_csr_level_stat *host_buf,
  * bfs_csr_run_host then (1) re-uploads the CSR from h_row_ptr/h_col when they
  * are non-NULL (same n and nnz; checked again when validation is on) and
  * re-derives the per-vertex data create builds from it (the degree-0 bitmap
- * and the head array: one pass over the rows), (2)
+ * and the probe array: one pass over the rows), (2)
  * runs the search, (3) copies dist, parent (if h_parent != NULL) and the level
  * count back, and synchronises `stream` before returning the run's status.
  * Pinned host memory makes the copies asynchronous and fast.
@@ -296,7 +344,7 @@ int bfs_csr_last_cuda_error(bfs_csr_handle h);
  *
  * Instead of a handle and a workspace it uses one scratch array that lives
  * in the library's own device memory (a file-scope __device__ array, about
- * 38 MB, held on every GPU that loads the library until the process exits).
+ * 33 MB, held on every GPU that loads the library until the process exits).
  * That bounds the graph: n <= 1,048,576 vertices and an int32 row_ptr
  * (nnz < 2^31); larger inputs are rejected with BFS_CSR_EUNSUPPORTED before
  * any work. The caller still provides the device CSR (d_row_ptr: n + 1

@@ -58,6 +58,7 @@ int main(void) {
   F(bfs_csr_options, grid_blocks); F(bfs_csr_options, barrier_timeout_ns);
   F(bfs_csr_options, test_unreachable_barrier); F(bfs_csr_options, push_beta);
   F(bfs_csr_options, narrow_max_edges); F(bfs_csr_options, lanes);
+  F(bfs_csr_options, parent_pass); F(bfs_csr_options, frontier_output);
   F(bfs_csr_options, reserved);
   F(bfs_csr_level_stat, level); F(bfs_csr_level_stat, direction); F(bfs_csr_level_stat, advance);
   F(bfs_csr_level_stat, frontier); F(bfs_csr_level_stat, frontier_edges);
@@ -93,9 +94,10 @@ def test_defaults(fbc):
     assert o.direction == fbc.BFS_CSR_DIR_AUTO and o.advance == fbc.BFS_CSR_ADV_AUTO
     assert o.discovery == fbc.BFS_CSR_DISC_BITMAP and o.loop_mode == fbc.BFS_CSR_LOOP_PERSISTENT
     assert (o.small_max_degree, o.cta_min_degree) == (32, 256)
-    assert o.merge_path_min_frontier == 4096  # Gunrock paper's static hybrid threshold
+    assert o.merge_path_min_frontier == 0     # the pages' hybrid threshold 4096 is an option
     assert o.pull_alpha == 14.0 and o.push_beta == 24
     assert o.max_depth == -1 and o.validate == 1 and o.lanes == 1
+    assert o.parent_pass == fbc.BFS_CSR_PARENT_AUTO
     assert o.barrier_timeout_ns > 0 and o.test_unreachable_barrier == 0
 
 
@@ -108,7 +110,10 @@ def test_workspace_sizing(fbc):
     n = 1 << 20
     assert fbc.workspace_bytes(n, 16 * n, False) >= n * (8 + 16)
     assert fbc.workspace_bytes(n, 16 * n, True) >= n * (8 + 32)
-    # every lane adds one search part; the graph part (head array) is shared
+    # the padded frontier modes add two arrays of nnz int32 per lane
+    pad = fbc.workspace_bytes(n, 16 * n, False, fbc.default_options(frontier_output=2))
+    assert pad - fbc.workspace_bytes(n, 16 * n, False) >= 2 * 16 * n * 4
+    # every lane adds one search part; the graph part (probe array) is shared
     one = fbc.workspace_bytes(n, 16 * n, False, fbc.default_options(lanes=1))
     two = fbc.workspace_bytes(n, 16 * n, False, fbc.default_options(lanes=2))
     three = fbc.workspace_bytes(n, 16 * n, False, fbc.default_options(lanes=3))
@@ -132,6 +137,16 @@ def test_argument_checks_without_gpu(fbc):
     bad = fbc.default_options(block_threads=100)
     assert fbc.bfs_csr_workspace_bytes(10, 10, 0, ctypes.byref(bad), ctypes.byref(out)) == \
         fbc.BFS_CSR_EINVAL
+    for pp in (-1, 3):
+        bad = fbc.default_options(parent_pass=pp)
+        assert fbc.bfs_csr_workspace_bytes(10, 10, 0, ctypes.byref(bad), ctypes.byref(out)) == \
+            fbc.BFS_CSR_EINVAL
+        bad = fbc.default_options(frontier_output=pp)
+        assert fbc.bfs_csr_workspace_bytes(10, 10, 0, ctypes.byref(bad), ctypes.byref(out)) == \
+            fbc.BFS_CSR_EINVAL
+        bad = fbc.default_options(discovery=pp)
+        assert fbc.bfs_csr_workspace_bytes(10, 10, 0, ctypes.byref(bad), ctypes.byref(out)) == \
+            fbc.BFS_CSR_EINVAL
     for lanes in (-1, 9):
         bad = fbc.default_options(lanes=lanes)
         assert fbc.bfs_csr_workspace_bytes(10, 10, 0, ctypes.byref(bad), ctypes.byref(out)) == \

@@ -61,6 +61,11 @@ def check_against_oracle(fbc, g, sources, bfs=None, max_depth=-1, stats=True):
             got = [r["frontier"] for r in rec]
             assert got == sizes.tolist(), (g.name, s)
             assert sum(got) == reached
+            # m_F of every level (after a pull level the kernel derives it
+            # from the edges the pull left unvisited)
+            deg = np.diff(g.row_ptr.astype(np.int64))
+            want_mf = [int(deg[want == k].sum()) for k in range(want_levels)]
+            assert [r["frontier_edges"] for r in rec] == want_mf, (g.name, s)
     if own:
         bfs.close()
 
@@ -187,10 +192,12 @@ def test_corner_cases(fbc):
 
 
 def test_distances_past_the_hop_byte(fbc):
-    """Distances of 254 and more do not fit the one-byte hop code and go to
-    dist directly; here they are reached by push and by pull levels: a
-    300-vertex path ends in a dense random cluster (so the automatic rule
-    pulls at depth ~300), plus isolated vertices; every direction mode."""
+    """Distances of 126 and more do not fit the hop code's 7 distance bits and
+    go to dist directly (the code's top bit flags a probe-neighbour parent);
+    here they are reached by push and by pull levels: a 300-vertex path ends
+    in a dense random cluster (so the automatic rule pulls at depth ~300),
+    plus isolated vertices; every direction mode, with parents stored at
+    discovery and written by the end-of-search pass."""
     rng = np.random.default_rng(17)
     path = 300
     cl = 4000
@@ -201,13 +208,14 @@ def test_distances_past_the_hop_byte(fbc):
     src += [path - 1] * 8 + a.tolist()
     dst += rng.integers(path, path + cl, 8).tolist() + b.tolist()
     g = graphgen.from_edges(path + cl + 50, src, dst, name="path_then_cluster")
-    for over in (dict(), dict(direction=1), dict(direction=2), dict(loop_mode=1)):
+    for over in (dict(), dict(direction=1), dict(direction=2), dict(loop_mode=1),
+                 dict(parent_pass=1), dict(parent_pass=1, direction=2)):
         bfs = fbc.BfsCsr(_dev(g.row_ptr), _dev(g.col), symmetric=True,
                          options=fbc.default_options(**over))
         check_against_oracle(fbc, g, [150, path + 5, 0], bfs=bfs)  # source 0 last: its records
         rec = bfs.level_stats()
         if over.get("direction", 0) != 1:
-            assert any(r["direction"] == fbc.BFS_CSR_DIR_PULL and r["level"] >= 254
+            assert any(r["direction"] == fbc.BFS_CSR_DIR_PULL and r["level"] >= 126
                        for r in rec), over
         bfs.close()
 
@@ -291,10 +299,22 @@ OPTION_MATRIX = [
     dict(grid_blocks=3, advance=1), dict(grid_blocks=7, advance=2, direction=1),
     dict(small_max_degree=1, cta_min_degree=2, advance=1),
     dict(small_max_degree=4, cta_min_degree=64, advance=1, direction=1),
-    dict(merge_path_min_frontier=0), dict(pull_alpha=0.0), dict(pull_alpha=1e9),
+    dict(merge_path_min_frontier=4096), dict(merge_path_min_frontier=4096, binned_max_degree=64),
+    dict(pull_alpha=0.0), dict(pull_alpha=1e9),
     dict(push_beta=0), dict(push_beta=1000000, pull_alpha=1.0),
     dict(narrow_max_edges=0), dict(narrow_max_edges=8), dict(narrow_max_edges=2048, advance=2),
     dict(narrow_max_edges=100000, block_threads=128), dict(narrow_max_edges=64, discovery=1),
+    dict(loop_mode=2), dict(loop_mode=2, direction=1, advance=1), dict(loop_mode=2, direction=2),
+    dict(loop_mode=2, discovery=1),
+    dict(parent_pass=1), dict(parent_pass=1, direction=2), dict(parent_pass=1, loop_mode=1),
+    dict(parent_pass=1, block_threads=64, grid_blocks=3), dict(parent_pass=2),
+    dict(parent_pass=1, discovery=1),
+    dict(discovery=2), dict(discovery=2, direction=1, advance=2), dict(discovery=2, direction=2),
+    dict(discovery=2, loop_mode=1, advance=1),
+    dict(frontier_output=1), dict(frontier_output=1, discovery=2),
+    dict(frontier_output=1, grid_blocks=3, direction=1), dict(frontier_output=2),
+    dict(frontier_output=2, discovery=2), dict(frontier_output=2, loop_mode=1, discovery=1),
+    dict(frontier_output=2, grid_blocks=1),
 ]
 
 
@@ -332,6 +352,58 @@ def test_depth_bound_with_level_records(fbc, depth):
                 assert rec[-1]["direction"] == 0 and rec[-1]["level"] == depth
                 assert rec[-1]["frontier"] == int((want == depth).sum())
             assert all(r["direction"] in (1, 2) for r in rec[:levels - 1])
+            bfs.close()
+
+
+def test_graph_loop_mode(fbc):
+    """The CUDA-graph level loop (a device-driven while node, one level per
+    body launch): the 2048 x 2048 grid (4,094 levels), a 3,000-level path,
+    the power-law graph from several sources into different outputs (one
+    graph per output set, reused on repeats), a depth bound, and a batch."""
+    opt = fbc.default_options(loop_mode=fbc.BFS_CSR_LOOP_GRAPH)
+    for g, srcs in ((graphgen.config(4), graphgen.config(4).sources[:1]),
+                    (graphgen.path_graph(3000), [0, 2999, 1500])):
+        bfs = fbc.BfsCsr(_dev(g.row_ptr), _dev(g.col), True, opt)
+        check_against_oracle(fbc, g, srcs, bfs=bfs)
+        bfs.close()
+    g = graphgen.config(1)
+    bfs = fbc.BfsCsr(_dev(g.row_ptr), _dev(g.col), True, opt)
+    outs = [torch.empty(g.n, dtype=torch.int32, device="cuda") for _ in range(3)]
+    for rep in range(3):
+        for i, s in enumerate(g.sources[:3]):
+            bfs.run(int(s), outs[i])
+            bfs.sync()
+    for i, s in enumerate(g.sources[:3]):
+        want = oracle.bfs(g.row_ptr, g.col, int(s), want_parent=False)[0]
+        assert np.array_equal(outs[i].cpu().numpy(), want)
+    bfs.close()
+    bfs = fbc.BfsCsr(_dev(g.row_ptr), _dev(g.col), True,
+                     fbc.default_options(loop_mode=fbc.BFS_CSR_LOOP_GRAPH, max_depth=3))
+    check_against_oracle(fbc, g, g.sources[:2], bfs=bfs, max_depth=3)
+    bfs.close()
+    dist, parent, levels = run_batch_rows(fbc, g, g.sources[:6], lanes=2,
+                                          loop_mode=fbc.BFS_CSR_LOOP_GRAPH)
+    check_rows_against_oracle(g, g.sources[:6], dist, parent, levels)
+
+
+def test_padded_frontier_records(fbc):
+    """The sentinel-padded frontier without a filter: every level is a push
+    level walked one thread per slot (advance code BFS_CSR_ADV_PADDED), and
+    with the filter a push level takes the merge path and never the
+    single-CTA mode; both agree with the oracle on the power-law graph and
+    the grid."""
+    for cfg in (1, 4):
+        g = graphgen.config(cfg)
+        for fo, disc in ((2, 2), (1, 2), (2, 0)):
+            bfs = fbc.BfsCsr(_dev(g.row_ptr), _dev(g.col), True,
+                             fbc.default_options(frontier_output=fo, discovery=disc))
+            check_against_oracle(fbc, g, g.sources[:2], bfs=bfs)
+            rec = bfs.level_stats()
+            if fo == 2:
+                assert all(r["direction"] == fbc.BFS_CSR_DIR_PUSH and
+                           r["advance"] == fbc.BFS_CSR_ADV_PADDED for r in rec)
+            else:
+                assert all(r["advance"] != fbc.BFS_CSR_ADV_SINGLE_CTA for r in rec)
             bfs.close()
 
 

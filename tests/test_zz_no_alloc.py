@@ -113,7 +113,9 @@ def test_noalloc_options_match_regular_entry_point(fbc, over):
 def test_noalloc_malformed_csr_then_recovers(fbc):
     """A malformed CSR is rejected by the validation pass with EINVAL; the
     next call on a good graph, on the same shared scratch, is still right.
-    Several lanes are refused: the scratch holds one search."""
+    Several lanes are refused (the scratch holds one search), and so are the
+    graph loop mode (a graph is a resource the entry point cannot keep) and
+    the padded frontiers (their arrays do not fit the scratch)."""
     g = graphgen.config(1)
     bad = g.row_ptr.copy()
     bad[10], bad[11] = bad[11], bad[10] - 1      # row_ptr decreases
@@ -123,5 +125,11 @@ def test_noalloc_malformed_csr_then_recovers(fbc):
     assert status == fbc.BFS_CSR_EINVAL
     status, *_ = _noalloc(fbc, torch.from_numpy(g.row_ptr).cuda(), col, g.n, g.nnz,
                           int(g.sources[0]), opt=fbc.default_options(lanes=2))
+    assert status == fbc.BFS_CSR_EUNSUPPORTED
+    status, *_ = _noalloc(fbc, torch.from_numpy(g.row_ptr).cuda(), col, g.n, g.nnz,
+                          int(g.sources[0]), opt=fbc.default_options(loop_mode=2))
+    assert status == fbc.BFS_CSR_EUNSUPPORTED
+    status, *_ = _noalloc(fbc, torch.from_numpy(g.row_ptr).cuda(), col, g.n, g.nnz,
+                          int(g.sources[0]), opt=fbc.default_options(frontier_output=1))
     assert status == fbc.BFS_CSR_EUNSUPPORTED
     _compare(fbc, g, g.sources[2:4])
