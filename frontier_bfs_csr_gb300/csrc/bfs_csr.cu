@@ -25,7 +25,7 @@ using fbc::Params;
 namespace {
 
 constexpr int kStatsCap = 1 << 16;
-constexpr int kDefaultBlock = 512;
+constexpr int kDefaultBlock = fbc::kLevelBlock;
 
 constexpr int kMaxLanes = 8;
 
@@ -174,7 +174,8 @@ int check_options(const bfs_csr_options& o)
     if (o.small_max_degree < 1 || o.cta_min_degree < o.small_max_degree) return BFS_CSR_EINVAL;
     if (o.merge_path_min_frontier < 0 || o.binned_max_degree < 1) return BFS_CSR_EINVAL;
     if (!(o.pull_alpha >= 0.0) || o.push_beta < 0) return BFS_CSR_EINVAL;
-    if (o.block_threads != 0 && (o.block_threads < 64 || o.block_threads > 512 || o.block_threads % 32))
+    if (o.block_threads != 0 &&
+        (o.block_threads < 64 || o.block_threads > fbc::kLevelBlock || o.block_threads % 32))
         return BFS_CSR_EINVAL;
     if (o.grid_blocks < 0 || o.barrier_timeout_ns <= 0 || o.narrow_max_edges < 0)
         return BFS_CSR_EINVAL;

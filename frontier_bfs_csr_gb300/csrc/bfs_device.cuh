@@ -66,7 +66,10 @@ __host__ __device__ constexpr int window_cap(int bd)
     return kItems * bd;
 }
 constexpr int kSlots = 4;        // rotating per-level counter slots
-constexpr int kMaxBlock = 1024;
+// Threads per CTA of the level kernel (its largest and default block): two
+// CTAs per SM, so the register file gives each thread 65536 / (2 * kLevelBlock)
+// registers.
+constexpr int kLevelBlock = 512;
 constexpr unsigned kFull = 0xffffffffu;
 
 // Counters describing one frontier F_k. Level k - 1 accumulates them (all
@@ -1029,7 +1032,9 @@ __device__ void push_padded(const Params<RowT>& p, int k, unsigned long long L, 
 
 constexpr int kHeadVerts = 4;    // probe tests per lane in flight
 constexpr int kPullVerts = 2;    // miss rows per lane in flight
-constexpr int kPullRounds = 6;   // two-entry probe rounds before the warp takes a row
+constexpr int kRoundEntries = 4; // entries of a row tested per round (in flight together)
+constexpr int kPullRounds = 4;   // rounds before the whole warp takes a row
+constexpr int kTailEntries = 1;  // entries per lane per step of the whole-warp row scan
 constexpr int kPullList = 1024;  // per-warp list of unvisited vertices
 constexpr int kPullWin = 128;    // visited-bitmap words per warp window (4,096 vertices)
 
@@ -1046,11 +1051,12 @@ constexpr int kPullWin = 128;    // visited-bitmap words per warp window (4,096 
 // stored in the probe array (read nearly sequentially, with the flag that
 // marks a one-entry row; kHeadVerts entries per lane in flight, so their
 // probe -> frontier-bitmap chains overlap); most rows found by a wide pull
-// level resolve there, never touch row_ptr or col, and need no parent store. Rows that miss are scanned in CSR order, two
-// entries per round and kPullVerts rows per lane; one still unresolved after
-// kPullRounds rounds is scanned by the whole warp, 32 entries per step, and
-// the lowest hitting lane gives the first frontier neighbour in CSR order, as
-// the per-lane scan does. The parent is thus the probe neighbour when it is
+// level resolve there, never touch row_ptr or col, and need no parent
+// store. Rows that miss are scanned in CSR order, kRoundEntries entries per
+// round and kPullVerts rows per lane; one still unresolved after kPullRounds
+// rounds is scanned by the whole warp, 32 * kTailEntries entries per step,
+// and the first hit in CSR order gives the first frontier neighbour, as the
+// per-lane scan does. The parent is thus the probe neighbour when it is
 // in F_k, else the first neighbour in F_k in CSR order. The warp is the only
 // writer of its words of the visited and next-frontier bitmaps, so no global
 // atomics are needed, and every next-frontier word is written, so that bitmap
@@ -1157,7 +1163,7 @@ __device__ void pull_list(const Params<RowT>& p, int k, Tally& t, int32_t* wlist
         }
         __syncwarp();
     }
-    // Phase 2: the misses' rows in CSR order, two entries per round.
+    // Phase 2: the misses' rows in CSR order, kRoundEntries entries per round.
     for (int base = 0; base < nmiss; base += 32 * kPullVerts) {
         int32_t v[kPullVerts], par[kPullVerts], deg[kPullVerts];
         RowT cur[kPullVerts], end[kPullVerts];
@@ -1182,40 +1188,41 @@ __device__ void pull_list(const Params<RowT>& p, int k, Tally& t, int32_t* wlist
                 any |= par[b] < 0 && cur[b] < end[b];
             if (!__any_sync(kFull, any))
                 break;
-            int32_t u0[kPullVerts], u1[kPullVerts];
-            uint32_t f0[kPullVerts], f1[kPullVerts];
+            int32_t u[kPullVerts][kRoundEntries];
+            uint32_t f[kPullVerts][kRoundEntries];
 #pragma unroll
             for (int b = 0; b < kPullVerts; ++b) {
-                u0[b] = -1;
-                u1[b] = -1;
-                if (par[b] < 0 && cur[b] < end[b]) {
-                    u0[b] = p.col[cur[b]];
-                    if (cur[b] + 1 < end[b])
-                        u1[b] = p.col[cur[b] + 1];
-                }
+                const bool open = par[b] < 0 && cur[b] < end[b];
+#pragma unroll
+                for (int j = 0; j < kRoundEntries; ++j)
+                    u[b][j] = open && cur[b] + j < end[b] ? p.col[cur[b] + j] : -1;
             }
 #pragma unroll
-            for (int b = 0; b < kPullVerts; ++b) {
-                f0[b] = u0[b] >= 0 ? ldcg(fcur + (u0[b] >> 5)) : 0u;
-                f1[b] = u1[b] >= 0 ? ldcg(fcur + (u1[b] >> 5)) : 0u;
-            }
+            for (int b = 0; b < kPullVerts; ++b)
+#pragma unroll
+                for (int j = 0; j < kRoundEntries; ++j)
+                    f[b][j] = u[b][j] >= 0 ? ldcg(fcur + (u[b][j] >> 5)) : 0u;
             bool more = false;
 #pragma unroll
             for (int b = 0; b < kPullVerts; ++b) {
-                if (u0[b] >= 0) {
-                    if ((f0[b] >> (u0[b] & 31)) & 1u)
-                        par[b] = u0[b];
-                    else if (u1[b] >= 0 && ((f1[b] >> (u1[b] & 31)) & 1u))
-                        par[b] = u1[b];
-                    else
-                        cur[b] += 2;
+                if (u[b][0] >= 0) {
+                    // the first of the round's entries (in CSR order) that hit
+#pragma unroll
+                    for (int j = kRoundEntries - 1; j >= 0; --j)
+                        if (u[b][j] >= 0 && ((f[b][j] >> (u[b][j] & 31)) & 1u))
+                            par[b] = u[b][j];
+                    if (par[b] < 0)
+                        cur[b] += kRoundEntries;
                 }
                 more |= par[b] < 0 && cur[b] < end[b];
             }
             if (!__any_sync(kFull, more))
                 break;
         }
-        // Rows still open: the whole warp scans 32 entries per step.
+        // Rows still open: the whole warp scans kTailEntries * 32 entries per
+        // step, entry q + 32 j + lane in lane `lane` (coalesced col loads, all
+        // col and frontier-bitmap loads of a step in flight together); the
+        // first hit in CSR order is the lowest lane of the lowest j that hit.
 #pragma unroll
         for (int b = 0; b < kPullVerts; ++b) {
             unsigned mm = __ballot_sync(kFull, par[b] < 0 && cur[b] < end[b]);
@@ -1225,17 +1232,24 @@ __device__ void pull_list(const Params<RowT>& p, int k, Tally& t, int32_t* wlist
                 const RowT cp = __shfl_sync(kFull, cur[b], src);
                 const RowT ce = __shfl_sync(kFull, end[b], src);
                 int32_t hitv = -1;
-                for (RowT q = cp; q < ce && hitv < 0; q += 32) {
-                    const RowT e = q + lane;
-                    int32_t u = -1;
-                    bool hit = false;
-                    if (e < ce) {
-                        u = p.col[e];
-                        hit = (ldcg(fcur + (u >> 5)) >> (u & 31)) & 1u;
+                for (RowT q = cp; q < ce && hitv < 0; q += 32 * kTailEntries) {
+                    int32_t u[kTailEntries];
+                    uint32_t f[kTailEntries];
+#pragma unroll
+                    for (int j = 0; j < kTailEntries; ++j) {
+                        const RowT e = q + 32 * j + lane;
+                        u[j] = e < ce ? p.col[e] : -1;
                     }
-                    const unsigned hm = __ballot_sync(kFull, hit);
-                    if (hm)
-                        hitv = __shfl_sync(kFull, u, __ffs(hm) - 1);
+#pragma unroll
+                    for (int j = 0; j < kTailEntries; ++j)
+                        f[j] = u[j] >= 0 ? ldcg(fcur + (u[j] >> 5)) : 0u;
+#pragma unroll
+                    for (int j = 0; j < kTailEntries; ++j) {
+                        const bool hit = u[j] >= 0 && ((f[j] >> (u[j] & 31)) & 1u);
+                        const unsigned hm = __ballot_sync(kFull, hit);
+                        if (hm != 0u && hitv < 0)
+                            hitv = __shfl_sync(kFull, u[j], __ffs(hm) - 1);
+                    }
                 }
                 if (lane == src) {
                     par[b] = hitv;
@@ -1762,7 +1776,7 @@ __host__ __device__ inline size_t level_smem_bytes(int bd)
 
 // The persistent level loop (S2-S9).
 template <typename RowT>
-__global__ void __launch_bounds__(512, 2) level_kernel(Params<RowT> p)
+__global__ void __launch_bounds__(kLevelBlock, 2) level_kernel(Params<RowT> p)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     __shared__ SmemScalars ss;
