@@ -646,13 +646,13 @@ def per_config(torch, fbc, graphgen, device, peak, rows_out, keep_rows=True):
 # name, options, (sources, timed repeats) when fewer than the default: the
 # thread-mapped padded advance walks a hub's whole row on one thread.
 ABLATION = [
-    ("auto_dir+merge_path(default)", dict(), None),
+    ("auto_dir+auto_adv(default)", dict(), None),
     ("push_only+auto_adv", dict(direction=1), None),
     ("pull_only", dict(direction=2), None),
     ("push_only+binned", dict(direction=1, advance=1), None),
     ("push_only+merge_path", dict(direction=1, advance=2), None),
     ("auto_dir+binned", dict(advance=1), None),
-    ("auto_dir+hybrid_4096", dict(merge_path_min_frontier=4096), None),
+    ("auto_dir+merge_path", dict(advance=2), None),
     ("discovery_cas", dict(discovery=1), None),
     ("discovery_atomic_min", dict(discovery=2), None),
     ("atomic_min+padded+filter", dict(discovery=2, frontier_output=1), None),
@@ -666,9 +666,10 @@ ABLATION = [
 
 def ablation(torch, fbc, graphgen, device, cases, nsrc=16, reps=3):
     """Direction (push only, pull only, the automatic rule), push advance
-    (degree-binned, merge path -- the default -- and the pages' static hybrid
-    that takes the merge path from a 4,096-vertex frontier or an 8,192-degree
-    hub), discovery (bitmap
+    (degree-binned, merge path, and the automatic choice: the pages' static
+    hybrid -- merge path from a 4,096-vertex frontier or an 8,192-degree hub
+    -- plus the merge path for frontiers whose rows average 8 entries or
+    more), discovery (bitmap
     atomicOr, atomicCAS, atomicMin on dist), the Gunrock-style padded frontier
     with and without its filter, and where parents are written, on the first
     16 sources of each config: one search at a time (lanes = 1), GTEPS of a
@@ -713,7 +714,7 @@ def ablation(torch, fbc, graphgen, device, cases, nsrc=16, reps=3):
             res[name] = {"gteps": round(sum(edge_rows[:kv]) / (ms * 1e-3) / 1e9, 2),
                          "ms_per_search": round(ms / kv, 4), "sources": kv, "timed": rv,
                          "same_dist_as_auto": same}
-        auto = res["auto_dir+merge_path(default)"]["gteps"]
+        auto = res["auto_dir+auto_adv(default)"]["gteps"]
         for name in res:
             res[name]["vs_auto"] = round(res[name]["gteps"] / auto, 3) if auto else None
         out[str(cfg)] = {"sources": k, "variants": res}

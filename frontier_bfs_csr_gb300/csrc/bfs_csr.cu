@@ -25,7 +25,7 @@ using fbc::Params;
 namespace {
 
 constexpr int kStatsCap = 1 << 16;
-constexpr int kDefaultBlock = fbc::kLevelBlock;
+
 
 constexpr int kMaxLanes = 8;
 
@@ -102,7 +102,7 @@ struct bfs_csr_t {
     int device = 0;
     int sm_count = 0;
     int l2_bytes = 0;
-    int block = kDefaultBlock;
+    int block = 0;
     int grid = 0;
     size_t smem = 0;
     int last_cuda_error = 0;
@@ -175,7 +175,7 @@ int check_options(const bfs_csr_options& o)
     if (o.merge_path_min_frontier < 0 || o.binned_max_degree < 1) return BFS_CSR_EINVAL;
     if (!(o.pull_alpha >= 0.0) || o.push_beta < 0) return BFS_CSR_EINVAL;
     if (o.block_threads != 0 &&
-        (o.block_threads < 64 || o.block_threads > fbc::kLevelBlock || o.block_threads % 32))
+        (o.block_threads < 64 || o.block_threads > fbc::kLevelBlockMax || o.block_threads % 32))
         return BFS_CSR_EINVAL;
     if (o.grid_blocks < 0 || o.barrier_timeout_ns <= 0 || o.narrow_max_edges < 0)
         return BFS_CSR_EINVAL;
@@ -206,7 +206,9 @@ void* level_kernel_ptr() { return reinterpret_cast<void*>(&fbc::level_kernel<Row
 template <typename RowT>
 int configure_grid(bfs_csr_t* h)
 {
-    h->block = h->opt.block_threads ? h->opt.block_threads : kDefaultBlock;
+    h->block = h->opt.block_threads ? h->opt.block_threads : fbc::level_block<RowT>();
+    if (h->block > fbc::level_block<RowT>())
+        return BFS_CSR_EINVAL;  // above the kernel's launch bound for this row_ptr width
     h->smem = fbc::level_smem_bytes<RowT>(h->block);
     FBC_CUDA(h, cudaFuncSetAttribute(fbc::level_kernel<RowT>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h->smem));
@@ -573,7 +575,7 @@ int bfs_csr_default_options(bfs_csr_options* o)
     o->loop_mode = BFS_CSR_LOOP_PERSISTENT;
     o->small_max_degree = 32;
     o->cta_min_degree = 256;
-    o->merge_path_min_frontier = 0;
+    o->merge_path_min_frontier = 4096;
     o->binned_max_degree = 8192;
     o->pull_alpha = 14.0;
     o->push_beta = 24;

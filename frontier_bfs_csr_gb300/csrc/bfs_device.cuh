@@ -66,10 +66,24 @@ __host__ __device__ constexpr int window_cap(int bd)
     return kItems * bd;
 }
 constexpr int kSlots = 4;        // rotating per-level counter slots
-// Threads per CTA of the level kernel (its largest and default block): two
-// CTAs per SM, so the register file gives each thread 65536 / (2 * kLevelBlock)
-// registers.
-constexpr int kLevelBlock = 512;
+// Threads per CTA of the level kernel (its largest and default block), two
+// CTAs per SM, so the register file gives each thread 65536 / (2 * block)
+// registers: 384 threads (80 registers, no spills) with 4-byte row offsets,
+// 512 threads (64 registers) with 8-byte ones. Measured on GB300: 384 is
+// 8-12 % faster on the graphs of up to 2^22 vertices, 512 is 4-5 % faster on
+// R-MAT scale 25 with two searches in flight.
+template <typename RowT>
+__host__ __device__ constexpr int level_block()
+{
+    return sizeof(RowT) == 4 ? 384 : 512;
+}
+constexpr int kLevelBlockMax = 512;
+
+// A push level below the merge-path frontier threshold still takes the merge
+// path when its rows average at least this many entries: short rows (a
+// lattice's) are walked fastest one thread per vertex, longer ones are
+// balanced better edge by edge.
+constexpr long long kMergePathMinAvgDegree = 8;
 constexpr unsigned kFull = 0xffffffffu;
 
 // Counters describing one frontier F_k. Level k - 1 accumulates them (all
@@ -1776,7 +1790,7 @@ __host__ __device__ inline size_t level_smem_bytes(int bd)
 
 // The persistent level loop (S2-S9).
 template <typename RowT>
-__global__ void __launch_bounds__(kLevelBlock, 2) level_kernel(Params<RowT> p)
+__global__ void __launch_bounds__(level_block<RowT>(), 2) level_kernel(Params<RowT> p)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     __shared__ SmemScalars ss;
@@ -1803,6 +1817,9 @@ __global__ void __launch_bounds__(kLevelBlock, 2) level_kernel(Params<RowT> p)
         const unsigned long long found = ldcg_u64(&cur->found);
         const unsigned long long fedges = ldcg_u64(&cur->fedges);
         const unsigned long long maxdeg = ldcg_u64(&cur->maxdeg);
+        // F_k's queue counter, final here unless this level builds the queue
+        // from the frontier bitmap (then it is read again after that pass)
+        const unsigned long long qpack0 = ldcg_u64(&cur->qpack);
         const long long uprev = ldcg(&prv->unvisited);
         const long long ueprev = ldcg(&prv->unvisited_edges);
         const int prev_dir = ldcg(&prv->dir);
@@ -1862,9 +1879,8 @@ __global__ void __launch_bounds__(kLevelBlock, 2) level_kernel(Params<RowT> p)
         // alone; everyone meets at the barrier and resumes where it stopped.
         if (dir == BFS_CSR_DIR_PUSH && prev_dir != BFS_CSR_DIR_PULL && p.narrow_max > 0 &&
             p.level_budget == INT_MAX && p.frontier_output == BFS_CSR_FRONTIER_COMPACT) {
-            const unsigned long long qp0 = ldcg_u64(&cur->qpack);
-            const int qn0 = (int)(qp0 >> p.eb);
-            const long long qm0 = (long long)(qp0 & ((1ull << p.eb) - 1ull));
+            const int qn0 = (int)(qpack0 >> p.eb);
+            const long long qm0 = (long long)(qpack0 & ((1ull << p.eb) - 1ull));
             if (qm0 <= (long long)p.narrow_max && qn0 < sm.wcap) {
                 if (blockIdx.x == 0)
                     solo_levels(p, k, qn0, (RowT)qm0, F, U, mU, maxdeg, sm, ss, target,
@@ -1886,7 +1902,7 @@ __global__ void __launch_bounds__(kLevelBlock, 2) level_kernel(Params<RowT> p)
                 cur->adv = 0;
             }
             if (prev_dir != BFS_CSR_DIR_PULL) {
-                const int qn = (int)(ldcg_u64(&cur->qpack) >> p.eb);
+                const int qn = (int)(qpack0 >> p.eb);
                 queue_to_bitmap_clear(p, k);
                 if (!grid_barrier(p, target)) break;
                 queue_to_bitmap_set(p, k, qn);
@@ -1904,12 +1920,13 @@ __global__ void __launch_bounds__(kLevelBlock, 2) level_kernel(Params<RowT> p)
             // After a pull level that started with few unvisited vertices
             // (uprev is that count) the queue of F_k was built as it found
             // them; otherwise it is built from the frontier bitmap now.
+            unsigned long long qp = qpack0;
             if (prev_dir == BFS_CSR_DIR_PULL && uprev > p.emit_max) {
                 bitmap_to_queue(p, k, sm, ss, cur);
                 if (!grid_barrier(p, target)) break;
                 md = ldcg_u64(&cur->maxdeg);
+                qp = ldcg_u64(&cur->qpack);
             }
-            const unsigned long long qp = ldcg_u64(&cur->qpack);
             const int qn = (int)(qp >> p.eb);
             const RowT qm = (RowT)(qp & ((1ull << p.eb) - 1ull));
             if (p.frontier_output == BFS_CSR_FRONTIER_PADDED)
@@ -1921,7 +1938,8 @@ __global__ void __launch_bounds__(kLevelBlock, 2) level_kernel(Params<RowT> p)
             else if (p.advance == BFS_CSR_ADV_MERGE_PATH)
                 adv = BFS_CSR_ADV_MERGE_PATH;
             else
-                adv = (qn >= p.mp_min_frontier || md >= (unsigned long long)p.binned_max_deg)
+                adv = (qn >= p.mp_min_frontier || md >= (unsigned long long)p.binned_max_deg ||
+                       (long long)qm >= kMergePathMinAvgDegree * (long long)qn)
                           ? BFS_CSR_ADV_MERGE_PATH : BFS_CSR_ADV_BINNED;
             if (leader) {
                 LevelSlot* z = &p.ctl->slot[(k + 2) & 3];

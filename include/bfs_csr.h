@@ -47,10 +47,10 @@ extern "C" {
 
 /* Load balance of a top-down (push) level. */
 #define BFS_CSR_ADV_AUTO 0      /* merge-path when |F| >= merge_path_min_frontier
-                                   or the largest frontier degree >= binned_max_degree,
-                                   else binned (the Gunrock paper's static hybrid; with
-                                   the default threshold 0 every push level takes the
-                                   merge path, measured at least as fast here) */
+                                   (the Gunrock paper's static hybrid threshold), when
+                                   the largest frontier degree >= binned_max_degree, or
+                                   when the frontier's rows average 8 entries or more;
+                                   binned otherwise */
 #define BFS_CSR_ADV_BINNED 1    /* thread / warp / CTA per vertex by degree */
 #define BFS_CSR_ADV_MERGE_PATH 2 /* edge-balanced: degree prefix + search */
 #define BFS_CSR_ADV_SINGLE_CTA 3 /* (level records only) a narrow level run by one CTA */
@@ -106,15 +106,17 @@ typedef struct bfs_csr_options {
     int32_t loop_mode;               /* BFS_CSR_LOOP_*, default PERSISTENT */
     int32_t small_max_degree;        /* binned: degree < this -> thread per vertex (32) */
     int32_t cta_min_degree;          /* binned: degree >= this -> CTA per vertex (256) */
-    int32_t merge_path_min_frontier; /* auto advance threshold on |F| (0; the pages'
-                                        hybrid uses 4096) */
+    int32_t merge_path_min_frontier; /* auto advance threshold on |F| (4096) */
     int32_t binned_max_degree;       /* auto advance threshold on max degree (8192) */
     double pull_alpha;               /* auto direction after a push level: pull iff
                                         m_F * pull_alpha > m_U, the edges of the vertices
                                         not reached yet (14) */
     int32_t max_depth;               /* label only vertices within this many hops; <0: all */
     int32_t validate;                /* nonzero: check the CSR at create (O(nnz)) */
-    int32_t block_threads;           /* CTA size of the level kernel; 0 = default (512) */
+    int32_t block_threads;           /* CTA size of the level kernel, a multiple of 32 from
+                                        64; 0 = default and largest: 384 with int32
+                                        row_ptr, 512 with int64 (create fails with
+                                        BFS_CSR_EINVAL above it) */
     int32_t grid_blocks;             /* CTAs of the level kernel; 0 = fill every SM */
     int64_t barrier_timeout_ns;      /* limit of any device-wide wait (10 s) */
     int32_t test_unreachable_barrier;/* diagnostics only: nonzero makes the first

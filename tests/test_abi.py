@@ -94,7 +94,7 @@ def test_defaults(fbc):
     assert o.direction == fbc.BFS_CSR_DIR_AUTO and o.advance == fbc.BFS_CSR_ADV_AUTO
     assert o.discovery == fbc.BFS_CSR_DISC_BITMAP and o.loop_mode == fbc.BFS_CSR_LOOP_PERSISTENT
     assert (o.small_max_degree, o.cta_min_degree) == (32, 256)
-    assert o.merge_path_min_frontier == 0     # the pages' hybrid threshold 4096 is an option
+    assert o.merge_path_min_frontier == 4096  # Gunrock paper's static hybrid threshold
     assert o.pull_alpha == 14.0 and o.push_beta == 24
     assert o.max_depth == -1 and o.validate == 1 and o.lanes == 1
     assert o.parent_pass == fbc.BFS_CSR_PARENT_AUTO

@@ -299,7 +299,7 @@ OPTION_MATRIX = [
     dict(grid_blocks=3, advance=1), dict(grid_blocks=7, advance=2, direction=1),
     dict(small_max_degree=1, cta_min_degree=2, advance=1),
     dict(small_max_degree=4, cta_min_degree=64, advance=1, direction=1),
-    dict(merge_path_min_frontier=4096), dict(merge_path_min_frontier=4096, binned_max_degree=64),
+    dict(merge_path_min_frontier=0), dict(merge_path_min_frontier=100000, binned_max_degree=64),
     dict(pull_alpha=0.0), dict(pull_alpha=1e9),
     dict(push_beta=0), dict(push_beta=1000000, pull_alpha=1.0),
     dict(narrow_max_edges=0), dict(narrow_max_edges=8), dict(narrow_max_edges=2048, advance=2),
@@ -449,6 +449,10 @@ def test_errors(fbc):
     col[7] = g.n  # out of range
     with pytest.raises(fbc.BfsError) as e:
         fbc.BfsCsr(_dev(g.row_ptr), _dev(col), True)
+    assert e.value.status == fbc.BFS_CSR_EINVAL
+    # a CTA size above the level kernel's bound for int32 row offsets (384)
+    with pytest.raises(fbc.BfsError) as e:
+        fbc.BfsCsr(_dev(g.row_ptr), _dev(g.col), True, fbc.default_options(block_threads=512))
     assert e.value.status == fbc.BFS_CSR_EINVAL
     d = graphgen.random_graph(8, 0.4, 3, directed=True)
     bfs = fbc.BfsCsr(_dev(d.row_ptr), _dev(d.col), False, fbc.default_options(direction=2))
