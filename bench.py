@@ -256,7 +256,8 @@ def init_bytes_survey(n: int) -> int:
 
 def init_bytes_kernel(n: int, with_parent: bool = True) -> int:
     """This library's init kernel with bitmap discovery: one hop-code byte per
-    vertex, parent (-1), the visited bitmap written and the dead bitmap read."""
+    vertex, parent (-1) unless the end-of-search pass writes parents, the
+    visited bitmap written and the dead bitmap read."""
     words = (n + 31) // 32
     return (n + 15) // 16 * 16 + (4 * n if with_parent else 0) + 8 * words
 
@@ -426,7 +427,11 @@ def run_ours(args):
     lvl_bytes = sum(per_source[s]["survey_bytes"] for s in sources) * args.steps
     ker_bytes = sum(per_source[s]["kernel_bytes"] for s in sources) * args.steps
     achieved = lvl_bytes / (busy * 1e-3) / 1e9
-    init_b = init_bytes_kernel(n) * runs
+    # parents are written by the end pass (and not filled at init) when the
+    # parent array exceeds half of the L2
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    init_parent = 4 * n <= l2 // 2
+    init_b = init_bytes_kernel(n, with_parent=init_parent) * runs
     init_gbs = init_b / (sum(init_ms) * 1e-3) / 1e9
     run_bytes = (lvl_bytes + init_bytes_survey(n) * runs) / args.steps
 
@@ -469,7 +474,7 @@ def run_ours(args):
                          "what": "init (8n + n/4) plus level bytes per step over the step time"},
         "per_level": table,
         "init_kernel": {"achieved_gbs": round(init_gbs, 1), "frac": round(init_gbs / peak, 4),
-                        "bytes_per_launch": init_bytes_kernel(n),
+                        "bytes_per_launch": init_bytes_kernel(n, with_parent=init_parent),
                         "launch_ms_mean": round(sum(init_ms) / runs, 4)},
         "clocks": clocks,
         "gpu_launches": 2 * runs,
@@ -876,13 +881,43 @@ def run_e2e(torch, fbc, g, sources, args, device, ws):
         h.run_batch(sources, dist_np, par_np, lev_np, row_ptr=rp_np, col=col_np)
     elapsed = time.perf_counter() - t
     h.close()
+    del dist_t, par_t
     elapsed = max_over_ranks(torch, ws, elapsed, device)
     edges = sum_over_ranks(torch, ws, float(edges_per_step * steps), device)
+    h2d = int(g.row_ptr.nbytes + g.col.nbytes + 8 * k)
+    d2h = int(k * (8 * g.n + 4))
+    link = link_bandwidth(torch, device)
     return {"value": round(edges / elapsed / 1e9, 3), "unit": "GTEPS",
-            "h2d_bytes_per_step": int(g.row_ptr.nbytes + g.col.nbytes + 8 * k),
-            "d2h_bytes_per_step": int(k * (8 * g.n + 4)),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": steps, "ms_per_step": round(elapsed / steps * 1e3, 3),
-            "api": "bfs_csr_create_host / bfs_csr_run_host_batch"}
+            "api": "bfs_csr_create_host / bfs_csr_run_host_batch",
+            "host_link": dict(link, copy_floor_ms=round(
+                (h2d / link["h2d_gbs"] + d2h / link["d2h_gbs"]) / 1e6, 2))}
+
+
+def link_bandwidth(torch, device, nbytes: int = 1 << 30, reps: int = 3):
+    """Plain pinned-memory copies of one 1 GiB buffer each way (cudaMemcpyAsync
+    through torch, CUDA events, best of reps), outside any timed region: the
+    host link this box delivered, which bounds the end-to-end step."""
+    hbuf = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    dbuf = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    out = {}
+    for name in ("h2d", "d2h"):
+        best = float("inf")
+        for _ in range(reps):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            if name == "h2d":
+                dbuf.copy_(hbuf, non_blocking=True)
+            else:
+                hbuf.copy_(dbuf, non_blocking=True)
+            e1.record()
+            e1.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        out[name + "_gbs"] = round(nbytes / best / 1e6, 1)
+    del hbuf, dbuf
+    return out
 
 
 # ------------------------------------------------------------------ CPU leg

@@ -196,7 +196,13 @@ int bfs_csr_create(bfs_csr_handle *out, int64_t n, int64_t nnz,
                    const bfs_csr_options *opt, void *stream);
 
 /*
- * Enqueue one search from `source` on `stream`. d_dist (n int32, required),
+ * Enqueue one search from `source` on `stream`: the level-synchronous search
+ * of "100 Days of GPU, Day 38: Graph traversal on a GPU" (its host loop
+ * `runBfs`: reset, then one frontier expansion per level until a level
+ * discovers nothing) and of "The Frontier Model for Parallel Breadth-First
+ * Search" (ch. 22, sections 22.1-22.2: expand every frontier vertex's CSR
+ * row, claim each unvisited neighbour once, the claimed vertices form the
+ * next frontier), with the levels run on the device. d_dist (n int32, required),
  * d_parent (n int32, may be NULL) and d_num_levels (one int32, may be NULL:
  * the number of non-empty frontiers, i.e. the source's eccentricity + 1 when
  * no depth bound cuts it short) are caller-owned device memory. The call is
@@ -226,7 +232,12 @@ int bfs_csr_run_init(bfs_csr_handle h, int64_t source, int32_t *d_dist,
 int bfs_csr_run_levels(bfs_csr_handle h, int32_t *d_num_levels, void *stream);
 
 /* Wait for the handle's last run on `stream`; return its device status and
- * store the level count in *num_levels (may be NULL). */
+ * store the level count in *num_levels (may be NULL). This is the one
+ * device->host read a search needs: Day 38's `runBfs` reads the next
+ * frontier's size back after every level ("What a level-synchronous search
+ * actually launches"); here the level loop runs on the device and only its
+ * end state (status, done, level count) is read, once. A search that ended
+ * without reaching its end state gives BFS_CSR_EDEVICE. */
 int bfs_csr_sync(bfs_csr_handle h, void *stream, int32_t *num_levels);
 
 /*
@@ -253,7 +264,12 @@ int bfs_csr_run_batch(bfs_csr_handle h, int32_t num_sources, const int64_t *sour
                       int64_t *d_stamps, void *stream);
 
 /* Copy up to cap per-level records of the last synchronised run to host
- * memory; *count receives the number of levels the run had. */
+ * memory; *count receives the number of levels the run had. The records are
+ * the columns of the level table of "100 Days of GPU, Day 38" ("What a
+ * level-synchronous search actually launches": level, frontier size, edges,
+ * largest degree) plus the direction, advance, unvisited count and device
+ * timer stamps of each level; their frontier sizes sum to the reached count,
+ * the page's check against a vertex queued twice ("Pitfalls"). */
 int bfs_csr_level_stats(bfs_csr_handle h, bfs_csr_level_stat *host_buf,
                         int32_t cap, int32_t *count);
 
