@@ -994,8 +994,8 @@ def cpu_leg(g, timed_rows, config_rows, graphgen, budget_s: float = 20.0):
 def run_profile_case(args):
     """Small cases for a profiler (ncu), nothing timed or printed but a line
     of what ran. 'levels': 3 warm-up searches, then --sources searches of
-    --config in the host loop mode, so that every level is its own
-    level_kernel launch. 'walk': the power-law graph's hub level (the level
+    --config (or only those at --source-index) in the host loop mode, so
+    that every level is its own level_kernel launch. 'walk': the power-law graph's hub level (the level
     whose frontier holds the largest degree, most eccentric source) walked
     once by each mapping, 64 repeats."""
     import torch
@@ -1004,22 +1004,30 @@ def run_profile_case(args):
     import graphgen
     device = torch.device("cuda", 0)
     if args.profile == "levels":
-        g = graphgen.config(args.config)
+        if args.rmat_scale > 0:
+            g = graphgen.rmat(args.rmat_scale, 16, 7)
+            g.sources = graphgen.pick_sources(g, 24, 7)
+        else:
+            g = graphgen.config(args.config)
         row_ptr, col, _, _ = graph_tensors(torch, g, device)
         bfs = fbc.BfsCsr(row_ptr, col, True, fbc.default_options(loop_mode=fbc.BFS_CSR_LOOP_HOST))
         dist = torch.empty(g.n, dtype=torch.int32, device=device)
         parent = torch.empty_like(dist)
-        s0 = int(g.sources[0])
+        nsrc = args.sources if args.sources > 0 else 1
+        chosen = (g.sources[:nsrc] if not args.source_index else
+                  [g.sources[int(i)] for i in args.source_index.split(",")])
+        s0 = int(chosen[0])
+        warm_levels = 0
         for _ in range(3):
             bfs.run(s0, dist, parent)
-            bfs.sync()
-        nsrc = args.sources if args.sources > 0 else 1
+            warm_levels += bfs.sync()
         levels = []
-        for s in g.sources[:nsrc]:
+        for s in chosen:
             bfs.run(int(s), dist, parent)
             levels.append(bfs.sync())
         bfs.close()
-        print(json.dumps({"profile": "levels", "config": args.config, "warmup_searches": 3,
+        print(json.dumps({"profile": "levels", "graph": g.name, "warmup_searches": 3,
+                          "warmup_levels": warm_levels, "sources": [int(s) for s in chosen],
                           "levels_per_search": levels}))
         return
     g = graphgen.config(1)
@@ -1112,6 +1120,12 @@ def main():
                     help="searches bfs_csr_run_batch keeps in flight (1..8)")
     ap.add_argument("--sources", type=int, default=0,
                     help="use only the first S sources of the workload (0: all)")
+    ap.add_argument("--rmat-scale", type=int, default=0,
+                    help="--profile levels: an R-MAT graph of this scale (edge factor 16, "
+                         "seed 7, 24 sources drawn with seed 7) instead of --config")
+    ap.add_argument("--source-index", type=str, default="",
+                    help="--profile levels: search only the workload's sources at these "
+                         "indexes (comma-separated)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

@@ -51,7 +51,8 @@ constexpr int kItems = 4;        // edges per thread per single-CTA level round
 // Single-CTA level capacities, in entries. The stage holds the next frontier
 // (and is the CTA stage of the grid-wide compaction); a single-CTA level's
 // edges are bounded by it, so its winners always fit. The window holds the
-// current frontier. Both are one round of kItems edges per thread: a wider
+// current frontier. Both are one round of kItems entries per thread (the
+// window three with 8-byte row offsets, see window_cap): a wider
 // stage (7,168 entries with 4-byte row offsets, several rounds per level)
 // made the lattice's levels slower on one CTA than on the whole grid, and
 // its shared memory took L1 capacity from the other configurations.
@@ -61,9 +62,13 @@ __host__ __device__ constexpr int stage_cap(int bd)
     return kItems * bd;
 }
 
+template <typename RowT>
 __host__ __device__ constexpr int window_cap(int bd)
 {
-    return kItems * bd;
+    // three rounds for 8-byte row offsets, so that two CTAs' shared memory
+    // leaves the SM a 124 KB L1 (the window's frontier of single-CTA levels
+    // is then at most 3 * bd - 1 vertices)
+    return (sizeof(RowT) == 8 ? 3 : kItems) * bd;
 }
 constexpr int kSlots = 4;        // rotating per-level counter slots
 // Threads per CTA of the level kernel (its largest and default block), two
@@ -753,7 +758,7 @@ __device__ void push_binned(const Params<RowT>& p, int k, int qn, RowT qm, const
 // edge), so a window whose first entry holds e covers a whole item. Winners
 // go to the warp's own slice of the stage; a flush moves it to the next
 // queue with one packed atomic per warp.
-constexpr int kWarpStage = 256;  // stage entries per warp
+constexpr int kWarpStage = 224;  // stage entries per warp
 constexpr int kWItems = 4;       // 32-edge items per warp batch
 
 template <typename RowT>
@@ -1051,6 +1056,10 @@ constexpr int kPullRounds = 4;   // rounds before the whole warp takes a row
 constexpr int kTailEntries = 1;  // entries per lane per step of the whole-warp row scan
 constexpr int kPullList = 1024;  // per-warp list of unvisited vertices
 constexpr int kPullWin = 128;    // visited-bitmap words per warp window (4,096 vertices)
+// The list grows 32 visited words (up to 1,024 vertices) at a time, and its
+// entries are 16-bit offsets within the window.
+static_assert(kPullList >= 32 * 32, "one 32-word step must fit an empty list");
+static_assert(kPullWin * 32 <= 65536, "window offsets must fit 16 bits");
 
 // Pull level over the frontier bitmap fb[k & 1] (bit u set iff u is in F_k).
 // Every warp owns a contiguous range of visited-bitmap words and walks it in
@@ -1129,15 +1138,17 @@ __device__ __forceinline__ void emit_found(const Params<RowT>& p, int k, LevelSl
 }
 
 // One pass over the warp's list wlist[0, total) of unvisited vertices, all in
-// the window whose first visited-bitmap word is w0: phase 1 (probe tests)
-// then phase 2 (row scans of the misses). Found vertices get their bit in
-// wfound (indexed by word - w0).
+// the window whose first visited-bitmap word is w0, each held as its offset
+// from the window's first vertex 32 * w0 (a window spans 32 * kPullWin
+// vertices, so 16 bits): phase 1 (probe tests) then phase 2 (row scans of
+// the misses). Found vertices get their bit in wfound (indexed by word - w0).
 template <typename RowT>
-__device__ void pull_list(const Params<RowT>& p, int k, Tally& t, int32_t* wlist, int total,
+__device__ void pull_list(const Params<RowT>& p, int k, Tally& t, uint16_t* wlist, int total,
                           uint32_t* wfound, int w0)
 {
     const uint32_t* fcur = p.fb[k & 1];
     const int lane = threadIdx.x & 31;
+    const int32_t v0 = w0 << 5;
     // Phase 1: every list entry's probe neighbour, kHeadVerts per lane in
     // flight. Hits resolve here. A miss whose row is that one neighbour is
     // not found at this level (its one edge counts toward the unvisited
@@ -1152,7 +1163,7 @@ __device__ void pull_list(const Params<RowT>& p, int k, Tally& t, int32_t* wlist
 #pragma unroll
         for (int b = 0; b < kHeadVerts; ++b) {
             const int j = base + b * 32 + lane;
-            hv[b] = j < total ? wlist[j] : -1;
+            hv[b] = j < total ? v0 + (int32_t)wlist[j] : -1;
             hc[b] = hv[b] >= 0 ? __ldg(p.probe + hv[b]) : kProbeNone;
         }
 #pragma unroll
@@ -1172,7 +1183,7 @@ __device__ void pull_list(const Params<RowT>& p, int k, Tally& t, int32_t* wlist
             const bool miss = hv[b] >= 0 && !hit && u != kProbeNone && !(hc[b] >> 31);
             const unsigned mm = __ballot_sync(kFull, miss);
             if (miss)
-                wlist[nmiss + __popc(mm & ((1u << lane) - 1u))] = hv[b];
+                wlist[nmiss + __popc(mm & ((1u << lane) - 1u))] = (uint16_t)(hv[b] - v0);
             nmiss += __popc(mm);
         }
         __syncwarp();
@@ -1184,7 +1195,7 @@ __device__ void pull_list(const Params<RowT>& p, int k, Tally& t, int32_t* wlist
 #pragma unroll
         for (int b = 0; b < kPullVerts; ++b) {
             const int j = base + b * 32 + lane;
-            v[b] = j < nmiss ? wlist[j] : -1;
+            v[b] = j < nmiss ? v0 + (int32_t)wlist[j] : -1;
             par[b] = -1;
             cur[b] = 0;
             end[b] = 0;
@@ -1282,7 +1293,7 @@ __device__ void pull_list(const Params<RowT>& p, int k, Tally& t, int32_t* wlist
 }
 
 template <typename RowT>
-__device__ void pull_level(const Params<RowT>& p, int k, Tally& t, int32_t* wlist,
+__device__ void pull_level(const Params<RowT>& p, int k, Tally& t, uint16_t* wlist,
                            uint32_t* wfound, uint32_t* wvis, LevelSlot* emit)
 {
     uint32_t* fnext = p.fb[(k + 1) & 1];
@@ -1318,7 +1329,7 @@ __device__ void pull_level(const Params<RowT>& p, int k, Tally& t, int32_t* wlis
                     while (m) {
                         const int bit = __ffs(m) - 1;
                         m &= m - 1;
-                        wlist[pos++] = (w << 5) + bit;
+                        wlist[pos++] = (uint16_t)(((w - a) << 5) + bit);
                     }
                     nl += tot;
                     ++j;
@@ -1384,6 +1395,46 @@ __device__ void queue_to_bitmap_set(const Params<RowT>& p, int k, int qn)
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < qn; i += stride) {
         const int32_t v = ldcg(qv + i);
         atomicOr(f + (v >> 5), 1u << (v & 31));
+    }
+}
+
+// F_k from the hop codes: bit v of fb[k & 1] is set iff v's code holds
+// distance k (every vertex of F_k was recorded with that code by level k - 1;
+// codes are exact below kHopDirect). One coalesced pass that writes every
+// word, for large queues where an atomic per queued vertex costs more than
+// reading a byte per vertex; it also needs no clearing pass before it.
+__device__ __forceinline__ uint32_t hop_match4(uint32_t x, uint32_t code4)
+{
+    const uint32_t m = __vcmpeq4(x & 0x7f7f7f7fu, code4);  // 0xff per matching byte
+    return ((m >> 7) & 1u) | ((m >> 14) & 2u) | ((m >> 21) & 4u) | ((m >> 28) & 8u);
+}
+
+template <typename RowT>
+__device__ void hop_to_bitmap(const Params<RowT>& p, int k)
+{
+    uint32_t* f = p.fb[k & 1];
+    const uint32_t code = (uint32_t)(k + 1);
+    const uint32_t code4 = code * 0x01010101u;
+    const int full = p.n >> 5;  // words whose 32 vertices all exist
+    const uint4* h4 = reinterpret_cast<const uint4*>(p.hop);  // 256-byte aligned
+    const int stride = gridDim.x * blockDim.x;
+    for (int w = blockIdx.x * blockDim.x + threadIdx.x; w < p.words; w += stride) {
+        uint32_t bits = 0u;
+        if (w < full) {
+            const uint4 a = ldcg(h4 + 2 * w);
+            const uint4 b = ldcg(h4 + 2 * w + 1);
+            bits = hop_match4(a.x, code4) | hop_match4(a.y, code4) << 4 |
+                   hop_match4(a.z, code4) << 8 | hop_match4(a.w, code4) << 12 |
+                   hop_match4(b.x, code4) << 16 | hop_match4(b.y, code4) << 20 |
+                   hop_match4(b.z, code4) << 24 | hop_match4(b.w, code4) << 28;
+        } else {
+            for (int i = 0; i < 32; ++i) {
+                const int v = (w << 5) + i;
+                if (v < p.n && (uint32_t)(ldcg(p.hop + v) & 0x7f) == code)
+                    bits |= 1u << i;
+            }
+        }
+        __stcg(f + w, bits);
     }
 }
 
@@ -1763,7 +1814,7 @@ __device__ __forceinline__ Smem<RowT> carve_smem(unsigned char* raw, int bd)
     Smem<RowT> sm;
     unsigned char* q = raw;
     sm.cap = stage_cap<RowT>(bd);
-    sm.wcap = window_cap(bd) + 1;
+    sm.wcap = window_cap<RowT>(bd) + 1;
     sm.sb = reinterpret_cast<RowT*>(q); q += sizeof(RowT) * sm.cap;
     sm.sd = reinterpret_cast<int32_t*>(q); q += sizeof(int32_t) * sm.cap;
     sm.sv = reinterpret_cast<int32_t*>(q); q += sizeof(int32_t) * sm.cap;
@@ -1780,9 +1831,10 @@ __device__ __forceinline__ Smem<RowT> carve_smem(unsigned char* raw, int bd)
 template <typename RowT>
 __host__ __device__ inline size_t level_smem_bytes(int bd)
 {
-    const size_t scap = (size_t)stage_cap<RowT>(bd), wcap = (size_t)window_cap(bd);
+    const size_t scap = (size_t)stage_cap<RowT>(bd), wcap = (size_t)window_cap<RowT>(bd);
     const size_t push = (sizeof(RowT) + 8) * scap + (2 * sizeof(RowT) + 4) * (wcap + 1) + 16;
-    const size_t pull = (size_t)(bd / 32) * (kPullList + 2 * kPullWin) * sizeof(uint32_t);
+    const size_t pull = (size_t)(bd / 32) *
+                        (kPullList * sizeof(uint16_t) + 2 * kPullWin * sizeof(uint32_t));
     const size_t wstage = (size_t)(bd / 32) * kWarpStage * (sizeof(RowT) + 8);
     const size_t m = push > pull ? push : pull;
     return m > wstage ? m : wstage;
@@ -1903,16 +1955,22 @@ __global__ void __launch_bounds__(level_block<RowT>(), 2) level_kernel(Params<Ro
             }
             if (prev_dir != BFS_CSR_DIR_PULL) {
                 const int qn = (int)(qpack0 >> p.eb);
-                queue_to_bitmap_clear(p, k);
-                if (!grid_barrier(p, target)) break;
-                queue_to_bitmap_set(p, k, qn);
+                if (p.defer_dist && k + 1 < kHopDirect && 64ll * qn >= (long long)p.n) {
+                    hop_to_bitmap(p, k);
+                } else {
+                    queue_to_bitmap_clear(p, k);
+                    if (!grid_barrier(p, target)) break;
+                    queue_to_bitmap_set(p, k, qn);
+                }
                 if (!grid_barrier(p, target)) break;
             }
             {
                 const int wid = threadIdx.x >> 5;
-                int32_t* wlist = reinterpret_cast<int32_t*>(smem_raw) + wid * kPullList;
-                uint32_t* wfound = reinterpret_cast<uint32_t*>(smem_raw) +
-                                   (blockDim.x >> 5) * kPullList + wid * 2 * kPullWin;
+                uint16_t* wlist = reinterpret_cast<uint16_t*>(smem_raw) + wid * kPullList;
+                uint32_t* wfound =
+                    reinterpret_cast<uint32_t*>(smem_raw + (size_t)(blockDim.x >> 5) * kPullList *
+                                                               sizeof(uint16_t)) +
+                    wid * 2 * kPullWin;
                 pull_level(p, k, t, wlist, wfound, wfound + kPullWin,
                            U <= p.emit_max ? nxt : nullptr);
             }
