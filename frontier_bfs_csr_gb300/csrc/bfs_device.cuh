@@ -1101,40 +1101,101 @@ __device__ __forceinline__ void pull_resolve(const Params<RowT>& p, int k, Tally
     t.found += 1;
 }
 
-// Warp-collective: the lanes with `found` append their vertex to the queue
-// of F_{k+1} (slot nxt, queue (k + 1) & 1) with one packed atomic for the
-// warp; slot order and degree-prefix order agree as in the CTA stage.
+// The finds of one window (wfound, words a .. a + nwin) appended to the queue
+// of F_{k+1} (slot nxt, queue (k + 1) & 1). They are gathered as 16-bit
+// window offsets into the warp's list (free once the window's passes are
+// done), at most kPullList at a time; a first pass loads their rows' starts
+// and degrees with kEmitBatch loads per lane in flight and sums them, one
+// packed atomic reserves the list's slots and edge range, and a second pass
+// (its loads served by L1) writes the entries. Slot order and degree-prefix
+// order agree as in the CTA stage.
+constexpr int kEmitBatch = 4;
+
 template <typename RowT>
-__device__ __forceinline__ void emit_found(const Params<RowT>& p, int k, LevelSlot* nxt,
-                                           int32_t v, bool found)
+__device__ void emit_window(const Params<RowT>& p, int k, LevelSlot* nxt,
+                            const uint32_t* wfound, int a, int nwin, uint16_t* wlist)
 {
-    if (__ballot_sync(kFull, found) == 0u)
-        return;
     const int lane = threadIdx.x & 31;
-    RowT b = 0, deg = 0;
-    if (found) {
-        b = p.row_ptr[v];
-        deg = p.row_ptr[v + 1] - b;
+    uint32_t fw[kPullWin / 32];
+    int cnt = 0;
+#pragma unroll
+    for (int jj = 0; jj < kPullWin / 32; ++jj) {
+        const int i = 32 * jj + lane;
+        fw[jj] = i < nwin ? wfound[i] : 0u;
+        cnt += __popc(fw[jj]);
     }
-    const bool take = found && deg > 0;
-    const unsigned tm = __ballot_sync(kFull, take);
-    const unsigned long long d = take ? (unsigned long long)deg : 0ull;
-    const unsigned long long inc = warp_inclusive_scan(d);
-    const unsigned long long tot = __shfl_sync(kFull, inc, 31);
-    const unsigned long long md = warp_max(d);
-    unsigned long long old = 0ull;
-    if (lane == 0 && tm != 0u) {
-        old = atomicAdd(&nxt->qpack, ((unsigned long long)__popc(tm) << p.eb) | tot);
-        atomicMax(&nxt->maxdeg, md);
+    const int incl = warp_inclusive_scan(cnt);
+    const int tot = __shfl_sync(kFull, incl, 31);
+    const int32_t v0 = a << 5;
+    const int qs = (k + 1) & 1;
+    const unsigned long long emask = (1ull << p.eb) - 1ull;
+    for (int b0 = 0; b0 < tot; b0 += kPullList) {
+        int pos = incl - cnt;
+        __syncwarp();
+#pragma unroll
+        for (int jj = 0; jj < kPullWin / 32; ++jj) {
+            uint32_t f = fw[jj];
+            while (f != 0u) {
+                const int bit = __ffs(f) - 1;
+                f &= f - 1u;
+                if (pos >= b0 && pos < b0 + kPullList)
+                    wlist[pos - b0] = (uint16_t)(((32 * jj + lane) << 5) + bit);
+                ++pos;
+            }
+        }
+        __syncwarp();
+        const int m = min(kPullList, tot - b0);
+        unsigned long long edges = 0ull, md = 0ull;
+        int taken = 0;
+        for (int j0 = 0; j0 < m; j0 += 32 * kEmitBatch) {
+            RowT bb[kEmitBatch], ee[kEmitBatch];
+#pragma unroll
+            for (int u = 0; u < kEmitBatch; ++u) {
+                const int j = j0 + 32 * u + lane;
+                const int32_t v = j < m ? v0 + (int32_t)wlist[j] : -1;
+                bb[u] = v >= 0 ? p.row_ptr[v] : (RowT)0;
+                ee[u] = v >= 0 ? p.row_ptr[v + 1] : (RowT)0;
+            }
+#pragma unroll
+            for (int u = 0; u < kEmitBatch; ++u) {
+                const unsigned long long deg = (unsigned long long)(ee[u] - bb[u]);
+                if (deg > 0ull) {
+                    edges += deg;
+                    md = deg > md ? deg : md;
+                    ++taken;
+                }
+            }
+        }
+        edges = warp_sum(edges);
+        md = warp_max(md);
+        taken = warp_sum(taken);
+        unsigned long long old = 0ull;
+        if (lane == 0 && taken > 0) {
+            old = atomicAdd(&nxt->qpack, ((unsigned long long)taken << p.eb) | edges);
+            atomicMax(&nxt->maxdeg, md);
+        }
+        old = __shfl_sync(kFull, old, 0);
+        unsigned long long slot = old >> p.eb, run = old & emask;
+        for (int j0 = 0; j0 < m; j0 += 32) {
+            const int j = j0 + lane;
+            const int32_t v = j < m ? v0 + (int32_t)wlist[j] : -1;
+            const RowT b = v >= 0 ? p.row_ptr[v] : (RowT)0;
+            const RowT deg = v >= 0 ? p.row_ptr[v + 1] - b : (RowT)0;
+            const bool take = deg > 0;
+            const unsigned tm = __ballot_sync(kFull, take);
+            const unsigned long long d = take ? (unsigned long long)deg : 0ull;
+            const unsigned long long inc = warp_inclusive_scan(d);
+            if (take) {
+                const unsigned long long sl = slot + __popc(tm & ((1u << lane) - 1u));
+                p.qv[qs][sl] = v;
+                p.qbeg[qs][sl] = b;
+                p.qoff[qs][sl] = (RowT)(run + inc - d);
+            }
+            slot += __popc(tm);
+            run += __shfl_sync(kFull, inc, 31);
+        }
     }
-    old = __shfl_sync(kFull, old, 0);
-    if (take) {
-        const int qs = (k + 1) & 1;
-        const unsigned long long slot = (old >> p.eb) + __popc(tm & ((1u << lane) - 1u));
-        p.qv[qs][slot] = v;
-        p.qbeg[qs][slot] = b;
-        p.qoff[qs][slot] = (RowT)((old & ((1ull << p.eb) - 1ull)) + inc - d);
-    }
+    __syncwarp();
 }
 
 // One pass over the warp's list wlist[0, total) of unvisited vertices, all in
@@ -1346,19 +1407,9 @@ __device__ void pull_level(const Params<RowT>& p, int k, Tally& t, uint16_t* wli
                 break;
         }
         // Few unvisited vertices at the level's start: the window's finds also
-        // go to the next queue, a warp's worth of vertices per step.
-        if (emit != nullptr) {
-            for (int jj = 0; jj < kPullWin / 32; ++jj) {
-                const int i = 32 * jj + lane;
-                uint32_t f = i < nwin ? wfound[i] : 0u;
-                while (__any_sync(kFull, f != 0u)) {
-                    const bool has = f != 0u;
-                    const int bit = has ? __ffs(f) - 1 : 0;
-                    f &= f - 1u;
-                    emit_found(p, k, emit, ((a + i) << 5) + bit, has);
-                }
-            }
-        }
+        // go to the next queue.
+        if (emit != nullptr)
+            emit_window(p, k, emit, wfound, a, nwin, wlist);
 #pragma unroll
         for (int jj = 0; jj < kPullWin / 32; ++jj) {
             const int i = 32 * jj + lane;
