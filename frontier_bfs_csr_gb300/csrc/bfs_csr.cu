@@ -34,7 +34,7 @@ constexpr int kMaxLanes = 8;
 // are `search` bytes further on.
 struct Layout {
     size_t dead, probe;
-    size_t ctl, visited, hop, fb0, fb1, qv0, qv1, qbeg0, qbeg1, qoff0, qoff1, stats, pad0, pad1;
+    size_t ctl, visited, hop, fb0, fb1, qv0, qv1, qbeg0, qbeg1, qoff0, qoff1, wq, stats, pad0, pad1;
     size_t pad_entries;
     size_t search, total;
 };
@@ -68,6 +68,7 @@ Layout make_layout(int64_t n, int row_ptr_64, int lanes = 1, size_t pad_entries 
     L.qbeg1 = take((size_t)n * R);
     L.qoff0 = take((size_t)n * R);
     L.qoff1 = take((size_t)n * R);
+    L.wq = take((size_t)n * 4);
     L.stats = take((size_t)kStatsCap * sizeof(bfs_csr_level_stat));
     L.pad_entries = pad_entries;
     L.pad0 = pad_entries ? take(pad_entries * 4) : 0;
@@ -260,6 +261,7 @@ Params<RowT> make_params(bfs_csr_t* h, int32_t* d_dist, int32_t* d_parent, int32
     p.ctl = reinterpret_cast<Ctl*>(w + h->L.ctl);
     p.frontier_output = h->opt.frontier_output;
     p.emit_max = 65536;
+    p.wq = reinterpret_cast<int32_t*>(w + h->L.wq);
     p.pad[0] = h->L.pad_entries ? reinterpret_cast<int32_t*>(w + h->L.pad0) : nullptr;
     p.pad[1] = h->L.pad_entries ? reinterpret_cast<int32_t*>(w + h->L.pad1) : nullptr;
     p.stats = reinterpret_cast<bfs_csr_level_stat*>(w + h->L.stats);
@@ -1084,7 +1086,7 @@ constexpr int64_t kNoAllocMaxN = BFS_CSR_NOALLOC_MAX_VERTICES;
 constexpr size_t kNoAllocBytes =
     (sizeof(Ctl) + 256) + 4 * ((size_t)kNoAllocMaxN / 8 + 256) +
     ((size_t)kNoAllocMaxN * 4 + 256) + ((size_t)kNoAllocMaxN + 256) +
-    2 * ((size_t)kNoAllocMaxN * 4 + 256) + 4 * ((size_t)kNoAllocMaxN * 4 + 256) +
+    3 * ((size_t)kNoAllocMaxN * 4 + 256) + 4 * ((size_t)kNoAllocMaxN * 4 + 256) +
     ((size_t)kStatsCap * sizeof(bfs_csr_level_stat) + 256);
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];

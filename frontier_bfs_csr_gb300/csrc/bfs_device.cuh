@@ -178,6 +178,7 @@ struct Params {
     // level; the padded modes use pad[] (max(nnz, 1) entries each).
     int frontier_output;
     int32_t* pad[2];
+    int32_t* wq;                // winners of a large push level, before their degrees
     // A pull level that starts with at most this many unvisited vertices also
     // appends what it finds to the next queue, so that a push level after it
     // needs no bitmap-to-queue pass.
@@ -815,7 +816,28 @@ __device__ void warp_flush(const Params<RowT>& p, const WarpStage<RowT>& ws, int
     __syncwarp();
 }
 
+// Large push levels (at least kIdsMinEdges frontier edges) keep the winners'
+// row offsets out of the claim chain: the merge path stages only the winners'
+// ids (ids_flush appends them to wq, counted in the next slot's work_next),
+// and after a grid barrier queue_from_ids loads their row offsets with many
+// loads in flight and builds the queue of F_{k+1}.
+constexpr long long kIdsMinEdges = 1ll << 20;
+
 template <typename RowT>
+__device__ void ids_flush(const Params<RowT>& p, const WarpStage<RowT>& ws, int n, LevelSlot* nxt)
+{
+    __syncwarp();
+    const int lane = threadIdx.x & 31;
+    unsigned int base = 0u;
+    if (lane == 0)
+        base = atomicAdd(&nxt->work_next, (unsigned int)n);
+    base = __shfl_sync(kFull, base, 0);
+    for (int i = lane; i < n; i += 32)
+        p.wq[base + i] = ws.v[i];
+    __syncwarp();
+}
+
+template <typename RowT, bool kIds>
 __device__ void push_warp_mp(const Params<RowT>& p, int k, int qn, RowT qm, unsigned char* raw,
                              LevelSlot* nxt, Tally& t, bool pre)
 {
@@ -896,7 +918,10 @@ __device__ void push_warp_mp(const Params<RowT>& p, int k, int qn, RowT qm, unsi
             continue;
         }
         if (cnt + 32 * n > kWarpStage) {
-            warp_flush(p, ws, cnt, nxt, ns);
+            if constexpr (kIds)
+                ids_flush(p, ws, cnt, nxt);
+            else
+                warp_flush(p, ws, cnt, nxt, ns);
             cnt = 0;
         }
         int32_t vv[kWItems], uu[kWItems];
@@ -936,38 +961,113 @@ __device__ void push_warp_mp(const Params<RowT>& p, int k, int qn, RowT qm, unsi
             e += 32 * n;
             continue;
         }
-        RowT wb[kWItems], we[kWItems];
+        if constexpr (kIds) {
+            // winners' ids only; their degrees come later (queue_from_ids)
 #pragma unroll
-        for (int j = 0; j < kWItems; ++j) {
-            wb[j] = 0;
-            we[j] = 0;
-            if (won[j]) {
-                wb[j] = p.row_ptr[vv[j]];
-                we[j] = p.row_ptr[vv[j] + 1];
+            for (int j = 0; j < kWItems; ++j) {
+                if (won[j])
+                    t.found += 1;
+                const unsigned m = __ballot_sync(kFull, won[j]);
+                if (won[j])
+                    ws.v[cnt + __popc(m & ((1u << lane) - 1u))] = vv[j];
+                cnt += __popc(m);
             }
-        }
+        } else {
+            RowT wb[kWItems], we[kWItems];
 #pragma unroll
-        for (int j = 0; j < kWItems; ++j) {
-            const RowT deg = we[j] - wb[j];
-            if (won[j]) {
-                t.found += 1;
-                t.edges += (unsigned long long)deg;
-                t.maxdeg = (unsigned long long)deg > t.maxdeg ? (unsigned long long)deg : t.maxdeg;
+            for (int j = 0; j < kWItems; ++j) {
+                wb[j] = 0;
+                we[j] = 0;
+                if (won[j]) {
+                    wb[j] = p.row_ptr[vv[j]];
+                    we[j] = p.row_ptr[vv[j] + 1];
+                }
             }
-            const bool take = won[j] && deg > 0;
-            const unsigned m = __ballot_sync(kFull, take);
-            if (take) {
-                const int pos = cnt + __popc(m & ((1u << lane) - 1u));
-                ws.v[pos] = vv[j];
-                ws.b[pos] = wb[j];
-                ws.d[pos] = (int32_t)deg;
+#pragma unroll
+            for (int j = 0; j < kWItems; ++j) {
+                const RowT deg = we[j] - wb[j];
+                if (won[j]) {
+                    t.found += 1;
+                    t.edges += (unsigned long long)deg;
+                    t.maxdeg = (unsigned long long)deg > t.maxdeg ? (unsigned long long)deg
+                                                                  : t.maxdeg;
+                }
+                const bool take = won[j] && deg > 0;
+                const unsigned m = __ballot_sync(kFull, take);
+                if (take) {
+                    const int pos = cnt + __popc(m & ((1u << lane) - 1u));
+                    ws.v[pos] = vv[j];
+                    ws.b[pos] = wb[j];
+                    ws.d[pos] = (int32_t)deg;
+                }
+                cnt += __popc(m);
             }
-            cnt += __popc(m);
         }
         e += 32 * n;
     }
-    if (cnt > 0)
-        warp_flush(p, ws, cnt, nxt, ns);
+    if (cnt > 0) {
+        if constexpr (kIds)
+            ids_flush(p, ws, cnt, nxt);
+        else
+            warp_flush(p, ws, cnt, nxt, ns);
+    }
+}
+
+// The queue of F_{k+1} from the winners' ids in wq (nxt->work_next of them):
+// every warp takes an even share, loads kIdsBatch ids and their row offsets
+// per lane at a time, stages the vertices with edges and flushes them with
+// the packed atomic of the merge path. Adds the degrees to the tally (the
+// push level counted the winners).
+template <typename RowT>
+__device__ void queue_from_ids(const Params<RowT>& p, int k, unsigned char* raw, LevelSlot* nxt,
+                               Tally& t)
+{
+    constexpr int kIdsBatch = 4;
+    const long long total = (long long)ldcg(&nxt->work_next);
+    const long long W = (long long)gridDim.x * (blockDim.x >> 5);
+    const long long gw = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const long long lo = total * gw / W, hi = total * (gw + 1) / W;
+    const WarpStage<RowT> ws = warp_stage<RowT>(raw);
+    const int lane = threadIdx.x & 31;
+    const int ns = (k + 1) & 1;
+    for (long long c0 = lo; c0 < hi; c0 += kWarpStage) {
+        const int m = (int)(hi - c0 < kWarpStage ? hi - c0 : kWarpStage);
+        int cnt = 0;
+        for (int j0 = 0; j0 < m; j0 += 32 * kIdsBatch) {
+            int32_t v[kIdsBatch];
+            RowT b[kIdsBatch], e[kIdsBatch];
+#pragma unroll
+            for (int u = 0; u < kIdsBatch; ++u) {
+                const int j = j0 + 32 * u + lane;
+                v[u] = j < m ? ldcg(p.wq + c0 + j) : -1;
+            }
+#pragma unroll
+            for (int u = 0; u < kIdsBatch; ++u) {
+                b[u] = v[u] >= 0 ? p.row_ptr[v[u]] : (RowT)0;
+                e[u] = v[u] >= 0 ? p.row_ptr[v[u] + 1] : (RowT)0;
+            }
+#pragma unroll
+            for (int u = 0; u < kIdsBatch; ++u) {
+                const RowT deg = e[u] - b[u];
+                const bool take = v[u] >= 0 && deg > 0;
+                if (take) {
+                    t.edges += (unsigned long long)deg;
+                    t.maxdeg = (unsigned long long)deg > t.maxdeg ? (unsigned long long)deg
+                                                                  : t.maxdeg;
+                }
+                const unsigned tm = __ballot_sync(kFull, take);
+                if (take) {
+                    const int pos = cnt + __popc(tm & ((1u << lane) - 1u));
+                    ws.v[pos] = v[u];
+                    ws.b[pos] = b[u];
+                    ws.d[pos] = (int32_t)deg;
+                }
+                cnt += __popc(tm);
+            }
+        }
+        if (cnt > 0)
+            warp_flush(p, ws, cnt, nxt, ns);
+    }
 }
 
 // ------------------------------------------------------------ padded frontiers
@@ -2066,8 +2166,15 @@ __global__ void __launch_bounds__(level_block<RowT>(), 2) level_kernel(Params<Ro
             if (adv == BFS_CSR_ADV_PADDED) {
                 // qm is the length of the padded frontier here
                 push_padded(p, k, qp & ((1ull << p.eb) - 1ull), nxt, t, pre);
+            } else if (adv == BFS_CSR_ADV_MERGE_PATH &&
+                       p.frontier_output == BFS_CSR_FRONTIER_COMPACT &&
+                       (long long)qm >= kIdsMinEdges) {
+                push_warp_mp<RowT, true>(p, k, qn, qm, smem_raw, nxt, t, pre);
+                // every winner's id is in wq before its row offsets are read
+                if (!grid_barrier(p, target)) break;
+                queue_from_ids(p, k, smem_raw, nxt, t);
             } else if (adv == BFS_CSR_ADV_MERGE_PATH) {
-                push_warp_mp(p, k, qn, qm, smem_raw, nxt, t, pre);
+                push_warp_mp<RowT, false>(p, k, qn, qm, smem_raw, nxt, t, pre);
                 if (p.frontier_output == BFS_CSR_FRONTIER_PADDED_FILTER) {
                     // every slot of the padded output is written before the
                     // filter reads it

@@ -362,7 +362,7 @@ int bfs_csr_last_cuda_error(bfs_csr_handle h);
  *
  * Instead of a handle and a workspace it uses one scratch array that lives
  * in the library's own device memory (a file-scope __device__ array, about
- * 33 MB, held on every GPU that loads the library until the process exits).
+ * 37 MB, held on every GPU that loads the library until the process exits).
  * That bounds the graph: n <= 1,048,576 vertices and an int32 row_ptr
  * (nnz < 2^31); larger inputs are rejected with BFS_CSR_EUNSUPPORTED before
  * any work. The caller still provides the device CSR (d_row_ptr: n + 1

@@ -270,6 +270,34 @@ def test_config4_grid_corner(fbc):
     check_rows_against_oracle(g, g.sources[:1], dist, parent, levels)
 
 
+def test_large_level_paths_on_rmat22(fbc):
+    """The paths that only large levels take, shown to run and checked
+    against the oracle on R-MAT scale 22: with pushes only, merge-path levels
+    of at least 2^20 frontier edges (winners staged as ids, their queue built
+    after a grid barrier); by default, a pull level right after a push whose
+    queue holds at least n/64 vertices (frontier bitmap from the hop codes)."""
+    g = graphgen.config(3)
+    srcs = g.sources[:3]
+    for over, want in ((dict(direction=1, advance=2), "ids"), (dict(), "hop")):
+        bfs = fbc.BfsCsr(_dev(g.row_ptr), _dev(g.col), True, fbc.default_options(**over))
+        check_against_oracle(fbc, g, srcs, bfs=bfs)
+        seen = False
+        for s in srcs:
+            bfs.search(int(s))
+            rec = bfs.level_stats()
+            for a, b in zip(rec, rec[1:]):
+                if want == "ids":
+                    seen |= (a["direction"] == fbc.BFS_CSR_DIR_PUSH and
+                             a["advance"] == fbc.BFS_CSR_ADV_MERGE_PATH and
+                             a["frontier_edges"] >= 1 << 20)
+                else:
+                    seen |= (a["direction"] == fbc.BFS_CSR_DIR_PUSH and
+                             b["direction"] == fbc.BFS_CSR_DIR_PULL and
+                             64 * b["frontier"] >= g.n)
+        bfs.close()
+        assert seen, want
+
+
 def test_config5_rmat25_single_runs(fbc):
     """R-MAT scale 25 (int64 row_ptr) through single runs: dist, parent,
     level count and per-level records of two sources against the oracle."""
