@@ -1182,7 +1182,9 @@ static_assert(kPullWin * 32 <= 65536, "window offsets must fit 16 bits");
 // per-lane scan does. The parent is thus the probe neighbour when it is
 // in F_k, else the first neighbour in F_k in CSR order. The warp is the only
 // writer of its words of the visited and next-frontier bitmaps, so no global
-// atomics are needed, and every next-frontier word is written, so that bitmap
+// atomics are needed for them (a level that starts with at most emit_max
+// unvisited vertices also appends its finds to the next queue, one packed
+// atomic per window), and every next-frontier word is written, so that bitmap
 // needs no clearing.
 
 // x is found at level k with parent par. A parent that is x's probe
